@@ -1,0 +1,186 @@
+"""CPU oracle for attention over a block-paged KV cache (test infrastructure).
+
+This package is the slow, obviously correct definition that the CUDA library is
+checked against.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it; the
+product path never does, and it imports nothing from the product package.
+
+The arithmetic lives in ``pa_oracle.c`` (plain C, double precision, one key at a
+time through ``block_table``).  This module only builds that file with gcc and
+marshals numpy arrays into it.  bf16 tensors are passed as their raw uint16
+bits; outputs come back as float64.
+
+Sources: "大模型推理入门与 nano-vLLM 源码详解" §4.4, §9.2, §9.5, §11.2, §11.4,
+§13.1, §13.5, §19.1, §19.6; "大模型推理引擎入门 ... 对着日志读懂 nano-vllm"
+§2.7; Pico-vLLM log #6 ("VLLM on Fain的Blog").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpa_oracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+OK, INVALID, BOUNDS = 0, 1, 4
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c into a shared library with gcc (OpenMP if available)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # PA_ORACLE_LIB lets the mutation tests load a deliberately broken build
+            override = os.environ.get("PA_ORACLE_LIB")
+            lib = ctypes.CDLL(override if override else build())
+            i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+            lib.orc_kv_bytes_per_token.restype = i64
+            lib.orc_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
+            lib.orc_slot.restype = i64
+            lib.orc_slot.argtypes = [vp, i32, i64]
+            lib.orc_num_threads.restype = i32
+            lib.orc_set_num_threads.argtypes = [i32]
+            lib.orc_store_kvcache.restype = i32
+            lib.orc_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp]
+            pre = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32, dbl, vp]
+            lib.orc_prefill.restype = i32
+            lib.orc_prefill.argtypes = pre
+            lib.orc_prefill_weights.restype = i32
+            lib.orc_prefill_weights.argtypes = pre + [i32, i32, i32, vp]
+            lib.orc_decode.restype = i32
+            lib.orc_decode.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, dbl, vp]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _rows(a: np.ndarray, name: str):
+    """Validate a [T, H, d] bf16-bits array whose last two axes are packed;
+    return (array, token stride in elements)."""
+    if a.dtype != np.uint16 or a.ndim != 3:
+        raise OracleError(f"{name}: expected uint16 [T, H, d], got {a.dtype} {a.shape}")
+    if a.strides[2] != 2 or a.strides[1] != 2 * a.shape[2]:
+        a = np.ascontiguousarray(a)
+    if a.strides[0] % 2:
+        raise OracleError(f"{name}: token stride is not a whole number of elements")
+    return a, a.strides[0] // 2
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise OracleError(f"{what}: status {rc}")
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    return _load().orc_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes)
+
+
+def slot(block_table_row, block_size: int, pos: int) -> int:
+    row = _i32(block_table_row)
+    return _load().orc_slot(_ptr(row), block_size, pos)
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping):
+    """In-place KV write into (k_cache, v_cache) [NB, bs, Hkv, d] (uint16 bits).
+    Returns the oracle status (0, or 4 if some slot was out of range)."""
+    k, ks = _rows(k, "k")
+    v, vs = _rows(v, "v")
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or c.ndim != 4 or not c.flags.c_contiguous:
+            raise OracleError("cache must be a C-contiguous uint16 [NB, bs, Hkv, d] array")
+    slots = _i32(slot_mapping)
+    nb, bs, hkv, d = k_cache.shape
+    return _load().orc_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, d,
+                                     _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(slots))
+
+
+def prefill(q, cu_seqlens_q, cu_seqlens_k, scale, *, k=None, v=None, k_cache=None, v_cache=None,
+            block_table=None, weights_of=None):
+    """Causal varlen prefill; returns float64 [T, Hq, d] (and the weights of
+    row ``weights_of=(b, h, i)`` if asked).  With ``block_table=None`` keys come
+    from the contiguous ``k``/``v``; otherwise from the paged cache."""
+    q, qs = _rows(q, "q")
+    t, hq, d = q.shape
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    nseq = len(cu_q) - 1
+    if block_table is None:
+        k, kvs = _rows(k, "k")
+        v, vs2 = _rows(v, "v")
+        if kvs != vs2:
+            raise OracleError("k and v must share a token stride")
+        hkv = k.shape[1]
+        bt, mb, nb, bs, kc, vc = None, 0, 0, 1, None, None
+    else:
+        bt = _i32(block_table)
+        mb = bt.shape[1]
+        kc, vc = k_cache, v_cache
+        nb, bs, hkv, _ = kc.shape
+        kvs = 0
+        k = v = None
+    out = np.zeros((t, hq, d), dtype=np.float64)
+    lib = _load()
+    args = [_ptr(q), qs, _ptr(k), _ptr(v), kvs, _ptr(kc), _ptr(vc), nb, bs, _ptr(bt), mb,
+            _ptr(cu_q), _ptr(cu_k), nseq, hq, hkv, d, float(scale), _ptr(out)]
+    if weights_of is None:
+        _check(lib.orc_prefill(*args), "orc_prefill")
+        return out
+    b, h, i = weights_of
+    w = np.zeros(int(cu_k[b + 1] - cu_k[b]), dtype=np.float64)
+    _check(lib.orc_prefill_weights(*args, b, h, i, _ptr(w)), "orc_prefill_weights")
+    return out, w
+
+
+def decode(q, k_cache, v_cache, block_table, context_lens, scale):
+    """Paged decode: q [B, Hq, d] bits; returns float64 [B, Hq, d]."""
+    q, qs = _rows(q, "q")
+    b, hq, d = q.shape
+    bt, ctx = _i32(block_table), _i32(context_lens)
+    nb, bs, hkv, _ = k_cache.shape
+    out = np.zeros((b, hq, d), dtype=np.float64)
+    _check(_load().orc_decode(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(bt),
+                              bt.shape[1], _ptr(ctx), b, hq, hkv, d, float(scale), _ptr(out)),
+           "orc_decode")
+    return out

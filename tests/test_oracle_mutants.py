@@ -1,0 +1,47 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong index, a swapped operand ...), builds that copy on the CPU and
+runs the pin tests against it in a subprocess: every mutant must fail them.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pa_oracle.c")
+
+MUTANTS = {
+    "dropped_scale": ("scores[j] = scale * dot;", "scores[j] = dot;"),
+    "causal_off_by_one": ("h / group, p + 1,", "h / group, p,"),
+    "top_left_alignment": ("const int64_t p = (int64_t)lk - lq + i;", "const int64_t p = i;"),
+    "gqa_modulo_mapping": ("h / group, p + 1,", "h % kv_heads, p + 1,"),
+    "slot_without_block_size": ("block_table_row[pos / block_size] * block_size + pos % block_size",
+                                "block_table_row[pos / block_size] + pos % block_size"),
+    "unnormalised_weights": ("double w = exp(scores[j] - m) / denom;", "double w = exp(scores[j] - m);"),
+    "reads_k_for_v": ("out[e] += w * bf16_to_double(vj[e]);", "out[e] += w * bf16_to_double(kj[e]);"),
+    "decode_drops_new_token": ("&src, h / group, ctx,", "&src, h / group, ctx - 1,"),
+    "bf16_widening_shift": ("((uint32_t)bits) << 16;", "((uint32_t)bits) << 15;"),
+    "store_writes_k_to_v": ("v_cache[slot * row + e] = v[t * v_stride + e];",
+                            "v_cache[slot * row + e] = k[t * k_stride + e];"),
+    "store_drops_bounds_report": ("if (slot == -1) continue;", "if (slot < 0) continue;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new), encoding="utf-8")
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", str(mutant_c), "-o", str(lib), "-lm"],
+                   check=True, capture_output=True)
+    env = dict(os.environ, PA_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
