@@ -1,0 +1,544 @@
+"""Benchmark of the paged-attention hot path on one GB300 (or N replicas).
+
+A step is one decode step of the decode-batch workload through all 28 layers:
+for each layer, the KV write of the 256 new tokens into that layer's pool and
+paged decode attention of the 256 queries (256 sequences, context_lens
+U[100, 1024], block_size 256, 16 query / 8 KV heads x 128, bf16; every layer
+has its own pool, so the 28 pools, about 20 GB, never fit in L2).
+
+The JSON line reports:
+  value         algorithmic HBM bytes of the step (KV write + decode) / step
+                time, GB/s, device-resident inputs, CUDA events;
+  tokens_per_s  decode tokens per second (256 per step);
+  e2e           the same metric through the C ABI with inputs copied from
+                pinned host memory and outputs copied back inside the timed
+                region;
+  roofline      of the decode call (split + merge kernels), against the
+                measured HBM copy bandwidth;
+  prefill       the varlen-prefill (16384 packed tokens) and prefix+chunk
+                workloads: KV write + prefill, TFLOP/s of visible pairs;
+  long_decode   the 512-sequence, 4096-context decode, GB/s;
+  cpu_baseline  the CPU oracle on a bounded sample of the step's workload.
+
+``--impl reference`` times the CPU oracle alone on a bounded sample of the
+same workload, reporting the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_110_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attn HBM GB/s (% of ~8 TB/s); varlen prefill TFLOP/s; tokens/s"
+LAYERS = 28
+HQ, HKV, D = wl.HQ, wl.HKV, wl.HEAD_DIM
+ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
+
+# DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
+# valid only while the kernel source is unchanged.
+NCU_TRAFFIC = {"source_sha256": None, "bytes_per_call": None}
+
+
+def _file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ----------------------------------------------------------------- distributed
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_sum(world, t_max: float, units_sum: float):
+    """Max over ranks of the elapsed time, sum over ranks of the work done."""
+    if world == 1:
+        return t_max, units_sum
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    a = torch.tensor([t_max], dtype=torch.float64, device=dev)
+    b = torch.tensor([units_sum], dtype=torch.float64, device=dev)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(a.item()), float(b.item())
+
+
+# ----------------------------------------------------------------- algorithmic counts
+
+
+def decode_bytes(ctx, block_size, num_heads=HQ, kv_heads=HKV, head_dim=D):
+    """K+V rows read + q read + out written + table entries + context_lens."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    kv = int(ctx.sum()) * kv_heads * head_dim * 2 * 2
+    qo = len(ctx) * num_heads * head_dim * 2 * 2
+    tables = int((-(-ctx // block_size)).sum()) * 4 + len(ctx) * 4
+    return kv + qo + tables
+
+
+def store_bytes(num_tokens, kv_heads=HKV, head_dim=D):
+    """K and V rows read and written + the slot."""
+    return num_tokens * (kv_heads * head_dim * 2 * 2 * 2 + 4)
+
+
+def prefill_flops(query_lens, context_lens, num_heads=HQ, head_dim=D):
+    """4 * d * Hq per visible (query, key) pair (QK^T and PV, 2 flops each)."""
+    pairs = 0
+    for lq, lk in zip(np.asarray(query_lens, np.int64), np.asarray(context_lens, np.int64)):
+        off = lk - lq
+        pairs += lq * (off + 1) + lq * (lq - 1) // 2  # sum_{i<lq} (off + i + 1)
+    return 4 * head_dim * num_heads * int(pairs)
+
+
+# ----------------------------------------------------------------- peaks and clocks
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- the decode-batch step
+
+
+class DecodeStep:
+    """28 layers of (KV write of the new tokens, paged decode) over distinct
+    per-layer pools that share one set of block tables."""
+
+    def __init__(self, device, seed=wl.SEED_BASE + 2, layers=LAYERS, keep_host_layer0=False):
+        from paged_kv_cache_110_gb300 import binding as pa
+        self.pa = pa
+        self.dev = device
+        self.layers = layers
+        ctx = wl.rng(seed + 7).integers(100, 1024, size=256, endpoint=True).astype(np.int32)
+        self.ctx = ctx
+        self.layout = wl.make_layout(seed, ctx, 256)
+        self.B = len(ctx)
+        self.max_ctx = int(ctx.max())
+        self.k_cache, self.v_cache, self.tokens = [], [], []
+        self.host_layer0 = None
+        for l in range(layers):
+            kc, vc = wl.make_pool(self.layout, ctx - 1, seed + 1000 * (l + 1), device=device)
+            if l == 0 and keep_host_layer0:
+                self.host_layer0 = (wl.bf16_bits(kc).copy(), wl.bf16_bits(vc).copy())
+            self.k_cache.append(kc)
+            self.v_cache.append(vc)
+            self.tokens.append(wl.new_tokens(seed + 1000 * (l + 1) + 1, self.B, device=device))
+        self.slots_np = np.array([self.layout.slots(b, [c - 1])[0] for b, c in enumerate(ctx)], np.int32)
+        self.slots = torch.as_tensor(self.slots_np, device=device)
+        self.tables = torch.as_tensor(self.layout.block_tables, device=device)
+        self.ctx_t = torch.as_tensor(ctx, device=device)
+        n = pa.pa_decode_workspace_bytes(self.B, HQ, D, self.max_ctx)
+        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        self.out = [torch.empty((self.B, HQ, D), dtype=torch.bfloat16, device=device) for _ in range(layers)]
+        self.decode_bytes = decode_bytes(ctx, 256)
+        self.store_bytes = store_bytes(self.B)
+        self.step_bytes = layers * (self.decode_bytes + self.store_bytes)
+
+    def run(self, events=None):
+        pa = self.pa
+        for l in range(self.layers):
+            t = self.tokens[l]
+            pa.pa_store_kvcache(t.k, t.v, self.k_cache[l], self.v_cache[l], self.slots)
+            if events is not None:
+                events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                events[-1][0].record()
+            pa.pa_decode_paged(t.q, self.k_cache[l], self.v_cache[l], self.tables, self.ctx_t, self.max_ctx,
+                               wl.SCALE, self.out[l], self.ws)
+            if events is not None:
+                events[-1][1].record()
+
+    def launches_per_step(self):
+        splits = (self.max_ctx + 1) // 1  # placeholder, replaced below
+        del splits
+        return self.layers * (1 + (2 if self._multi_split() else 1))
+
+    def _multi_split(self):
+        # the library uses a merge kernel whenever a workspace is needed
+        return self.pa.pa_decode_workspace_bytes(self.B, HQ, D, self.max_ctx) > 0
+
+
+class E2EStep:
+    """The same step with host buffers: pinned host -> device copies of each
+    layer's new q/k/v and the step's metadata, the 28 layers, and the outputs
+    copied back, all inside the timed region."""
+
+    def __init__(self, step: DecodeStep):
+        self.s = step
+        self.h_qkv = [t.qkv.cpu().pin_memory() for t in step.tokens]
+        self.d_qkv = [torch.empty_like(t.qkv) for t in step.tokens]
+        self.h_slots = torch.as_tensor(step.slots_np).pin_memory()
+        self.h_tables = torch.as_tensor(step.layout.block_tables).pin_memory()
+        self.h_ctx = torch.as_tensor(step.ctx).pin_memory()
+        self.h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in step.out]
+        a, b = HQ * D, (HQ + HKV) * D
+        self.views = [(q[:, :a].view(-1, HQ, D), q[:, a:b].view(-1, HKV, D), q[:, b:].view(-1, HKV, D))
+                      for q in self.d_qkv]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_qkv) + \
+            sum(t.numel() * t.element_size() for t in (self.h_slots, self.h_tables, self.h_ctx))
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def run(self):
+        s, pa = self.s, self.s.pa
+        s.slots.copy_(self.h_slots, non_blocking=True)
+        s.tables.copy_(self.h_tables, non_blocking=True)
+        s.ctx_t.copy_(self.h_ctx, non_blocking=True)
+        for l in range(s.layers):
+            self.d_qkv[l].copy_(self.h_qkv[l], non_blocking=True)
+            q, k, v = self.views[l]
+            pa.pa_store_kvcache(k, v, s.k_cache[l], s.v_cache[l], s.slots)
+            pa.pa_decode_paged(q, s.k_cache[l], s.v_cache[l], s.tables, s.ctx_t, s.max_ctx, wl.SCALE, s.out[l], s.ws)
+            self.h_out[l].copy_(s.out[l], non_blocking=True)
+
+
+def time_region(fn, steps, world):
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        fn()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+# ----------------------------------------------------------------- prefill and long decode legs
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_prefill(device, steps, warmup, flush):
+    from paged_kv_cache_110_gb300 import binding as pa
+    res = {}
+    cases = {"varlen_16k": [wl.varlen_prefill(device=device)]}
+    a, b, _ = wl.prefix_chunk(device=device)
+    cases["prefix_2048_chunked"] = [a, b]
+    for name, calls in cases.items():
+        kc, vc = calls[0].k_cache, calls[0].v_cache
+        prepared = []
+        flops = 0
+        for c in calls:
+            out = torch.empty(c.tokens.q.shape, dtype=torch.bfloat16, device=device)
+            prepared.append((c, out, torch.as_tensor(c.slot_mapping, device=device),
+                             torch.as_tensor(c.block_tables, device=device),
+                             torch.as_tensor(c.cu_seqlens_q, device=device),
+                             torch.as_tensor(c.cu_seqlens_k, device=device)))
+            flops += prefill_flops(c.query_lens, c.context_lens)
+
+        def run(ev=None):
+            for c, out, sl, bt, cq, ck in prepared:
+                pa.pa_store_kvcache(c.tokens.k, c.tokens.v, kc, vc, sl)
+                if ev is not None:
+                    ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                    ev[-1][0].record()
+                pa.pa_prefill_paged(c.tokens.q, cq, ck, int(c.query_lens.max()), int(c.context_lens.max()),
+                                    c.scale, out, k_cache=kc, v_cache=vc, block_table=bt)
+                if ev is not None:
+                    ev[-1][1].record()
+
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            ev = []
+            run(ev)
+            torch.cuda.synchronize()
+            times.append(sum(s.elapsed_time(e) for s, e in ev) / 1e3)
+        t = statistics.median(times)
+        res[name] = {"tflops": flops / t / 1e12, "ms": t * 1e3, "gflop": flops / 1e9,
+                     "query_tokens": int(sum(c.num_tokens for c in calls)), "calls": len(calls)}
+    return res
+
+
+def time_long_decode(device, steps, warmup, flush):
+    from paged_kv_cache_110_gb300 import binding as pa
+    batch = wl.long_decode(device=device)
+    max_ctx = int(batch.context_lens.max())
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(512, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
+    out = torch.empty((512, HQ, D), dtype=torch.bfloat16, device=device)
+    bt = torch.as_tensor(batch.block_tables, device=device)
+    ctx = torch.as_tensor(batch.context_lens, device=device)
+    sl = torch.as_tensor(batch.slot_mapping, device=device)
+    pa.pa_store_kvcache(batch.tokens.k, batch.tokens.v, batch.k_cache, batch.v_cache, sl)
+    for _ in range(warmup):
+        pa.pa_decode_paged(batch.tokens.q, batch.k_cache, batch.v_cache, bt, ctx, max_ctx, batch.scale, out, ws)
+    times = []
+    for _ in range(steps):
+        flush_l2(flush)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        pa.pa_decode_paged(batch.tokens.q, batch.k_cache, batch.v_cache, bt, ctx, max_ctx, batch.scale, out, ws)
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) / 1e3)
+    t = statistics.median(times)
+    nbytes = decode_bytes(batch.context_lens, 256)
+    del batch
+    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512}
+
+
+# ----------------------------------------------------------------- CPU oracle baseline
+
+
+def oracle_sample(host_layer0, step_meta, target_s=10.0, max_layers=64):
+    """Run the CPU oracle (KV write + decode of the full 256-sequence layer)
+    on layer-0 inputs repeatedly for about target_s seconds; returns the
+    metric value, cores and a description of the sample."""
+    import oracle
+    kc0, vc0 = host_layer0
+    ctx, tables, slots, tokens = step_meta
+    k, v, q = (wl.bf16_bits(t) for t in (tokens.k, tokens.v, tokens.q))
+    done = 0
+    t0 = time.perf_counter()
+    while done < max_layers:
+        kc, vc = kc0.copy(), vc0.copy()
+        oracle.store_kvcache(k, v, kc, vc, slots)
+        oracle.decode(q, kc, vc, tables, ctx, wl.SCALE)
+        done += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    el = time.perf_counter() - t0
+    nbytes = done * (decode_bytes(ctx, 256) + store_bytes(len(ctx)))
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} layer(s) of the decode-batch step (KV write + decode of 256 sequences) in {el:.1f} s",
+            "seconds": el}
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle as the reference arm: each step is one layer of the
+    decode-batch workload (KV write + decode of all 256 sequences)."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    seed = wl.SEED_BASE + 2
+    ctx = wl.rng(seed + 7).integers(100, 1024, size=256, endpoint=True).astype(np.int32)
+    layout = wl.make_layout(seed, ctx, 256)
+    kc, vc = wl.make_pool(layout, ctx - 1, seed + 1000, device="cpu")
+    kc0, vc0 = wl.bf16_bits(kc).copy(), wl.bf16_bits(vc).copy()
+    toks = wl.new_tokens(seed + 1001, 256, device="cpu")
+    slots = np.array([layout.slots(b, [c - 1])[0] for b, c in enumerate(ctx)], np.int32)
+    k, v, q = (wl.bf16_bits(t) for t in (toks.k, toks.v, toks.q))
+
+    def one():
+        a, b = kc0.copy(), vc0.copy()
+        oracle.store_kvcache(k, v, a, b, slots)
+        oracle.decode(q, a, b, layout.block_tables, ctx, wl.SCALE)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    nbytes = args.steps * (decode_bytes(ctx, 256) + store_bytes(256))
+    val = nbytes / el / 1e9
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode batch, one layer per step: 256 seqs, context_lens U[100,1024], "
+                                   "block_size 256, 16q/8kv x 128, KV write + paged decode"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} layer(s) of the decode-batch step on the host cores"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", local)
+    peaks, peak_kind = measured_peaks()
+
+    step = DecodeStep(device, seed=wl.SEED_BASE + 2 + 10000 * rank, keep_host_layer0=(rank == 0))
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) if \
+        os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    events = []
+    with ClockSampler(gpu_index) as clocks:
+        elapsed = time_region(lambda: step.run(events), args.steps, world)
+    t_max, bytes_all = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
+    value = bytes_all / t_max / 1e9
+    decode_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
+    achieved = step.decode_bytes / decode_s / 1e9
+
+    e2e = E2EStep(step)
+    for _ in range(2):
+        e2e.run()
+    e2e_el = time_region(e2e.run, args.steps, world)
+    e2e_t, e2e_bytes = reduce_max_sum(world, e2e_el, float(step.step_bytes * args.steps))
+
+    src = os.path.join(ROOT, "paged_kv_cache_110_gb300", "csrc", "decode_paged.cu")
+    traffic = NCU_TRAFFIC["bytes_per_call"] if NCU_TRAFFIC["source_sha256"] == _file_sha(src) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode batch x 28 layers: 256 seqs, context_lens U[100,1024], block_size 256, "
+                               "16q/8kv x 128 bf16; per layer KV write of 256 tokens + paged decode",
+                   "layers": LAYERS, "seqs": step.B, "sum_context": int(step.ctx.sum()),
+                   "l2": "inputs larger than L2: 28 distinct layer pools (%.1f GB)" %
+                         (LAYERS * 2 * step.layout.num_blocks * 256 * ROW_BYTES / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": world * step.B * args.steps / t_max,
+        "hbm_frac_of_8tbs": value / 8000.0,
+        "gpu_launches": args.steps * step.launches_per_step(),
+        "e2e": {"value": e2e_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": e2e.h2d,
+                "d2h_bytes_per_step": e2e.d2h, "ms_per_step": e2e_t / args.steps * 1e3},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode_paged (split + merge kernels)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes_per_call": step.decode_bytes,
+                     "us_per_call": decode_s * 1e6},
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_extras:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        host0 = step.host_layer0
+        meta = (step.ctx, step.layout.block_tables, step.slots_np, step.tokens[0])
+        del step, e2e
+        torch.cuda.empty_cache()
+        pre = time_prefill(device, max(args.steps, 5), 3, flush)
+        for v in pre.values():
+            v["frac_of_bf16_peak"] = v["tflops"] / peaks["bf16_tflops"]
+        line["prefill"] = pre
+        torch.cuda.empty_cache()
+        ld = time_long_decode(device, max(args.steps, 5), 3, flush)
+        ld["frac"] = ld["gbs"] / peaks["hbm_gbs"]
+        line["long_decode"] = ld
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

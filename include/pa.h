@@ -1,0 +1,172 @@
+/*
+ * pa.h -- C ABI of libpa: attention over a block-paged KV cache on one GB300
+ * (sm_103a).
+ *
+ * The three calls are the three GPU steps of one attention layer in a
+ * nano-vLLM style engine ("大模型推理入门与 nano-vLLM 源码详解" §13.1-13.2 and
+ * §20.5.2; "nano-vllm 技术分析" §4.1 Attention): write the new tokens' K/V
+ * into the cache by slot_mapping, then either causal varlen prefill over
+ * cu_seqlens (reading cached prefix blocks through block_table) or decode of
+ * one query per sequence over context_lens keys.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory; scratch space is passed in.
+ *   - bf16 data (IEEE binary16 "brain float", 2 bytes), int32 metadata.
+ *   - head_dim must be 128; Hq / Hkv (the query heads per KV head) must be
+ *     1, 2, 4 or 8; Hkv must be 1, 2, 4 or 8; block_size must be a multiple
+ *     of 16 in [16, 1024].  Other shapes return PA_ERR_UNSUPPORTED.
+ *   - The per-layer cache layout is [num_blocks, block_size, Hkv, head_dim],
+ *     row-major: pool row `slot` starts at element slot * Hkv * head_dim
+ *     ("大模型推理入门与 nano-vLLM 源码详解" §11.5, the per-layer slice of the
+ *     [2, layers, num_blocks, block_size, Hkv, head_dim] pool).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  They never synchronise, never allocate, and launch
+ *     a grid whose shape depends only on the host arguments, so they can be
+ *     captured in a CUDA graph.
+ *   - Errors the host can see (null pointers, unsupported shapes, negative
+ *     sizes) are returned synchronously and nothing is launched.  A launch
+ *     failure returns PA_ERR_CUDA.  Errors only the device can see (a slot
+ *     or block id outside the pool, a -1 table entry inside a live context,
+ *     a context longer than the table or the stated maximum) are written to
+ *     *dev_status (if dev_status is not NULL) as the first nonzero pa_status
+ *     code; the offending row is skipped and the kernel still completes.
+ *     Kernels never trap.  The caller zeroes *dev_status before the call and
+ *     reads it after synchronising.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent arguments */
+    PA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels are built for */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    PA_ERR_BOUNDS = 4,      /* (device) an index outside the pool or the table */
+    PA_ERR_TIMEOUT = 5      /* (device) a bounded wait gave up */
+} pa_status;
+
+/* Static English text for a status code; never NULL. */
+const char *pa_status_string(int status);
+
+/* Version of this ABI, major * 100 + minor. */
+int pa_abi_version(void);
+
+/*
+ * KV-cache bytes per token position across a whole model:
+ * 2 (K and V) x layers x kv_heads x head_dim x elem_bytes
+ * ("大模型推理入门与 nano-vLLM 源码详解" §4.4; 114,688 for Qwen3-0.6B bf16).
+ * Returns 0 if any argument is not positive.
+ */
+size_t pa_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int elem_bytes);
+
+/*
+ * KV write ("大模型推理入门与 nano-vLLM 源码详解" §13.1; "nano-vllm 技术分析"
+ * §4.1 store_kvcache).  For every token t < num_tokens with
+ * s = slot_mapping[t] != -1, copy the num_kv_heads * head_dim bf16 values of
+ * k[t] to pool row s of k_cache, and those of v[t] to row s of v_cache.
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim] bf16; head rows are
+ *                 packed, consecutive tokens are k_stride_tok / v_stride_tok
+ *                 ELEMENTS apart (k and v may be column views of a fused
+ *                 QKV buffer).  Strides must be >= num_kv_heads * head_dim.
+ *   k_cache,      [num_blocks, block_size, num_kv_heads, head_dim] bf16,
+ *   v_cache       written in place.
+ *   slot_mapping  [num_tokens] int32; -1 marks a padding row (skipped).
+ *                 Any other value outside [0, num_blocks * block_size) sets
+ *                 PA_ERR_BOUNDS in *dev_status and that row is skipped.
+ *                 Live slots must be distinct (not checked).
+ * num_tokens == 0 is valid and launches nothing.  The copy is bit-exact.
+ */
+pa_status pa_store_kvcache(const void *k, int64_t k_stride_tok, const void *v, int64_t v_stride_tok,
+                           int64_t num_tokens, int num_kv_heads, int head_dim,
+                           void *k_cache, void *v_cache, int64_t num_blocks, int block_size,
+                           const int32_t *slot_mapping, int32_t *dev_status, void *stream);
+
+/*
+ * Causal varlen prefill ("大模型推理入门与 nano-vLLM 源码详解" §11.2, §13.2-13.3,
+ * §10.2; flash_attn_varlen_func as nano-vLLM calls it, §20.5.2.2).
+ * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and a key
+ * context of Lk_b = cu_seqlens_k[b+1] - cu_seqlens_k[b] positions; its
+ * Lq_b queries are the LAST Lq_b positions of that context, so query i may
+ * read keys 0 .. Lk_b - Lq_b + i (bottom-right causal alignment).  Query
+ * head h reads KV head h / (num_heads / num_kv_heads).
+ *
+ *   q             [Tq, num_heads, head_dim] bf16, token stride q_stride_tok
+ *                 elements; Tq = cu_seqlens_q[num_seqs].
+ *   block_table   NULL: keys come from k / v rows cu_seqlens_k[b] ..
+ *                 (token stride kv_stride_tok), which requires
+ *                 cu_seqlens_k == cu_seqlens_q (checked on the device:
+ *                 PA_ERR_INVALID_ARG in *dev_status) and max_seqlen_k ==
+ *                 max_seqlen_q (checked on the host).  k_cache/v_cache are
+ *                 then ignored and may be NULL.
+ *                 Otherwise [num_seqs, max_blocks_per_seq] int32: key j of
+ *                 sequence b is pool row block_table[b][j / block_size] *
+ *                 block_size + j % block_size of k_cache / v_cache (the
+ *                 caller ran pa_store_kvcache for this call's tokens first);
+ *                 k / v are ignored and may be NULL.
+ *   max_seqlen_q, max_seqlen_k   host-side upper bounds of Lq_b and Lk_b;
+ *                 they size the grid.  A sequence that exceeds them sets
+ *                 PA_ERR_BOUNDS and its rows beyond the bound are not computed.
+ *   scale         softmax scale applied to q.k (1/sqrt(head_dim) usually).
+ *   out           [Tq, num_heads, head_dim] bf16, packed.
+ * Sequences with Lq_b == 0 are skipped.  Lk_b < Lq_b sets PA_ERR_INVALID_ARG.
+ */
+pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok,
+                           const void *k, const void *v, int64_t kv_stride_tok,
+                           const void *k_cache, const void *v_cache, int64_t num_blocks, int block_size,
+                           const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int num_seqs,
+                           int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                           int head_dim, float scale, void *out, int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of scratch pa_decode_paged needs for these host-side sizes on the
+ * current device (it depends on the device's SM count).  Returns 0 when the
+ * arguments are invalid.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+/*
+ * Paged decode of one query per sequence ("大模型推理入门与 nano-vLLM 源码详解"
+ * §9.5, §11.4, §13.5; flash_attn_with_kvcache as nano-vLLM calls it).
+ * Sequence b attends with q[b] to keys 0 .. context_lens[b]-1 read through
+ * block_table[b] (context_lens counts the token written this step).
+ * Softmax statistics of key ranges ("splits") are merged exactly as in §9.5
+ * (maximum, exponent sum, weighted numerator), never per page.
+ *
+ *   q             [num_seqs, num_heads, head_dim] bf16, seq stride
+ *                 q_stride_seq elements.
+ *   block_table   [num_seqs, max_blocks_per_seq] int32 (-1 padded; only the
+ *                 first ceil(ctx / block_size) entries are read).
+ *   context_lens  [num_seqs] int32.  0 marks a padded row: its output is 0
+ *                 and nothing is read.  A value above max_context_len or
+ *                 max_blocks_per_seq * block_size sets PA_ERR_BOUNDS and the
+ *                 row's output is 0.
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid).
+ *   out           [num_seqs, num_heads, head_dim] bf16, packed.
+ *   workspace     device scratch of at least
+ *                 pa_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ *                 max_context_len) bytes, 256-byte aligned; its contents on
+ *                 entry do not matter.  Calls that overlap on the GPU must
+ *                 not share a workspace.
+ */
+pa_status pa_decode_paged(const void *q, int64_t q_stride_seq,
+                          const void *k_cache, const void *v_cache, int64_t num_blocks, int block_size,
+                          const int32_t *block_table, int max_blocks_per_seq,
+                          const int32_t *context_lens, int num_seqs, int max_context_len,
+                          int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

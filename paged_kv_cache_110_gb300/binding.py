@@ -1,0 +1,181 @@
+"""Python binding of libpa's C ABI (``include/pa.h``).
+
+Argument marshalling only: each function checks dtypes / devices, reads data
+pointers, strides and sizes from torch tensors, and calls the C entry point
+of the same name on the current CUDA stream.  All computation happens in the
+library's CUDA kernels; there is no fallback.  If ``libpa.so`` has not been
+built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
+    "pa_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+]
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {pa_status_string(status)} (status {status})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_build.LIB_PATH):
+        raise ImportError(f"libpa.so is not built ({_build.LIB_PATH}); run __graft_entry__.build() "
+                          "or python -m paged_kv_cache_110_gb300._build")
+    L = ctypes.CDLL(_build.LIB_PATH)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_status_string.argtypes = [i32]
+    L.pa_abi_version.restype = i32
+    L.pa_abi_version.argtypes = []
+    L.pa_kv_bytes_per_token.restype = sz
+    L.pa_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
+    L.pa_store_kvcache.restype = i32
+    L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_prefill_paged.restype = i32
+    L.pa_prefill_paged.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32,
+                                   i32, i32, i32, f32, vp, vp, vp]
+    L.pa_decode_workspace_bytes.restype = sz
+    L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.pa_decode_paged.restype = i32
+    L.pa_decode_paged.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp,
+                                  vp, sz, vp, vp]
+    return L
+
+
+lib = _load()
+
+
+def pa_status_string(status: int) -> str:
+    return lib.pa_status_string(int(status)).decode()
+
+
+def pa_abi_version() -> int:
+    return lib.pa_abi_version()
+
+
+def pa_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    return lib.pa_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes)
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bf16_rows(t: torch.Tensor, name: str):
+    """[N, H, 128] bf16 CUDA tensor with packed heads -> (H, row stride in elements)."""
+    if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA bf16 [N, H, D] tensor, got {t.dtype} {tuple(t.shape)} {t.device}")
+    if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name}: heads and dims must be packed (strides {t.stride()})")
+    return t.shape[1], t.stride(0)
+
+
+def _cache(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA bf16 [num_blocks, block_size, Hkv, D] tensor")
+    return t.shape
+
+
+def _i32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA int32 tensor")
+    return t
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+# ---------------------------------------------------------------- the C entry points
+
+
+def pa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stream=None):
+    """KV write: k/v [T, Hkv, 128] bf16 (token stride free), caches
+    [NB, bs, Hkv, 128], slot_mapping [T] int32 (-1 skips)."""
+    hkv, ks = _bf16_rows(k, "k")
+    _, vs = _bf16_rows(v, "v")
+    nb, bs, chk, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    if slot_mapping.numel() != k.shape[0] or v.shape[0] != k.shape[0] or chk != hkv:
+        raise ValueError("pa_store_kvcache: inconsistent shapes")
+    _check(lib.pa_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], _ptr(k_cache),
+                                _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status), _stream(stream)),
+           "pa_store_kvcache")
+
+
+def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, out, *, k=None, v=None,
+                     k_cache=None, v_cache=None, block_table=None, dev_status=None, stream=None):
+    """Causal varlen prefill.  With block_table=None keys come from k/v;
+    otherwise from the paged caches."""
+    hq, qs = _bf16_rows(q, "q")
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (q.shape[0], hq, q.shape[2]):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    _i32(cu_seqlens_q, "cu_seqlens_q")
+    _i32(cu_seqlens_k, "cu_seqlens_k")
+    nseq = cu_seqlens_q.numel() - 1
+    if block_table is None:
+        hkv, kvs = _bf16_rows(k, "k")
+        _, vs = _bf16_rows(v, "v")
+        if vs != kvs:
+            raise ValueError("k and v must share a token stride")
+        args = (_ptr(k), _ptr(v), kvs, None, None, 0, 16, None, 1)
+    else:
+        nb, bs, hkv, _ = _cache(k_cache, "k_cache")
+        _cache(v_cache, "v_cache")
+        _i32(block_table, "block_table")
+        if block_table.dim() != 2 or block_table.shape[0] != nseq:
+            raise ValueError("block_table must be [num_seqs, max_blocks]")
+        args = (None, None, 0, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table), block_table.shape[1])
+    _check(lib.pa_prefill_paged(_ptr(q), qs, *args, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
+                                int(max_seqlen_q), int(max_seqlen_k), hq, hkv, q.shape[2], float(scale), _ptr(out),
+                                _ptr(dev_status), _stream(stream)),
+           "pa_prefill_paged")
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int) -> int:
+    return lib.pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len)
+
+
+def pa_decode_paged(q, k_cache, v_cache, block_table, context_lens, max_context_len, scale, out, workspace,
+                    dev_status=None, stream=None):
+    """Paged decode: q [B, Hq, 128] (seq stride free), out [B, Hq, 128]
+    packed, workspace a CUDA uint8 tensor of pa_decode_workspace_bytes."""
+    hq, qs = _bf16_rows(q, "q")
+    nb, bs, hkv, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(block_table, "block_table")
+    _i32(context_lens, "context_lens")
+    b = q.shape[0]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (b, hq, d):
+        raise ValueError("out must be a contiguous bf16 [B, Hq, D] tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != b or context_lens.numel() != b:
+        raise ValueError("block_table / context_lens do not match q")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_decode_paged(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table),
+                               block_table.shape[1], _ptr(context_lens), b, int(max_context_len), hq, hkv, d,
+                               float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                               _stream(stream)),
+           "pa_decode_paged")

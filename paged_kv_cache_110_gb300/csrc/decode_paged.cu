@@ -1,0 +1,471 @@
+// decode_paged.cu -- split-KV paged decode: one query token per sequence over
+// its paged history, grouped by KV head.
+//
+// What it computes ("大模型推理入门与 nano-vLLM 源码详解" §9.5, §11.4, §19.6):
+// for sequence b with ctx = context_lens[b] keys and query head h reading
+// KV head g = h / G (G = Hq / Hkv),
+//     s_j = scale * q_h . k_j,  out_h = sum_j softmax(s)_j v_j,  j < ctx,
+// where key j lives in pool row block_table[b][j / bs] * bs + j % bs.
+// The keys are cut into "splits"; each split keeps (max, exponent sum,
+// unnormalised numerator) and the splits are merged with the same
+// statistics, never normalised page by page (§9.5, the 2-and-6 example).
+//
+// Layout of the work (GB300 design, not the pages'):
+//  * CTA = (sequence, split), 8 warps.  Warp w serves KV head w % Hkv and
+//    every (8 / Hkv)-th 16-token chunk of the split, so each K/V byte of the
+//    split is read from HBM exactly once and all G query heads of the group
+//    use it (the pages' Triton kernel re-read K/V once per query head).
+//  * Within a warp, lanes 0-15 and 16-31 each take one token row of 256 B
+//    per 16-byte load (lane c holds dims 8c..8c+7), so one warp load moves
+//    two full 256-byte rows.
+//  * Scores: each lane forms 8 tokens x G heads partial dot products over
+//    its 8 dims, then a transposing butterfly over the 16 lanes of its half
+//    (shuffle masks 8, 4, 2, 1 that halve the live values each step) leaves
+//    each lane with whole dot products, 8G values for the cost of about 8G
+//    shuffles instead of 32G.
+//  * Online softmax in base 2 (scale folded with log2 e), per chunk.
+//  * Splits with more than one part write fp32 partials to the workspace and
+//    a small merge kernel combines them; a single-split sequence is
+//    finalised in place.
+#include <cstdlib>
+
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int D = pa::kHeadDim;
+constexpr int NW = 8;          // warps per CTA
+constexpr int CHUNK = 16;      // tokens per warp iteration (8 per half-warp)
+constexpr unsigned FULL = 0xffffffffu;
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct DecodeParams {
+    const uint16_t *q;
+    int64_t q_stride;
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    int64_t num_blocks;
+    int block_size;
+    const int32_t *block_table;
+    int max_blocks;
+    const int32_t *context_lens;
+    int num_seqs;
+    int max_ctx;
+    int num_heads;
+    int kv_heads;
+    float scale_log2;
+    uint16_t *out;
+    float *ws_o;      // [num_seqs][max_splits][num_heads][D]
+    float2 *ws_ml;    // [num_seqs][max_splits][num_heads] (max, sum), base-2
+    int split_len;
+    int max_splits;
+    int32_t *status;
+};
+
+struct Plan {
+    int split_len;
+    int max_splits;
+};
+
+Plan make_plan(int num_seqs, int max_ctx)
+{
+    Plan p{CHUNK, 0};
+    if (num_seqs <= 0 || max_ctx <= 0) return p;
+    int split = 0;
+    if (const char *env = std::getenv("PA_DECODE_SPLIT_TOKENS")) split = std::atoi(env);
+    if (split <= 0) {
+        const int sms = pa::num_sms() > 0 ? pa::num_sms() : 152;
+        const long long target_ctas = 16LL * sms;
+        long long per_seq = (target_ctas + num_seqs - 1) / num_seqs;
+        if (per_seq < 1) per_seq = 1;
+        long long len = (max_ctx + per_seq - 1) / per_seq;
+        len = (len + 63) / 64 * 64;
+        split = int(len < 64 ? 64 : len);
+    }
+    split = (split + CHUNK - 1) / CHUNK * CHUNK;
+    p.split_len = split;
+    p.max_splits = (max_ctx + split - 1) / split;
+    return p;
+}
+
+size_t workspace_bytes(int num_seqs, int num_heads, const Plan &p)
+{
+    if (p.max_splits <= 1) return 0;
+    const size_t n = size_t(num_seqs) * p.max_splits * num_heads;
+    const size_t o_bytes = (n * D * sizeof(float) + 255) / 256 * 256;
+    return o_bytes + n * sizeof(float2);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
+{
+    f[0] = pa::bf16_lo(u.x); f[1] = pa::bf16_hi(u.x);
+    f[2] = pa::bf16_lo(u.y); f[3] = pa::bf16_hi(u.y);
+    f[4] = pa::bf16_lo(u.z); f[5] = pa::bf16_hi(u.z);
+    f[6] = pa::bf16_lo(u.w); f[7] = pa::bf16_hi(u.w);
+}
+
+// One transposing butterfly step over the 16 lanes of a half-warp: lanes
+// whose bit M is set keep the upper half of x, the others the lower half,
+// and each adds its partner's copy of the half it keeps.  With N == 1 it is
+// a plain butterfly sum.
+template <int N, int M>
+__device__ __forceinline__ void xpose_step(float (&x)[8 * 8], int c)
+{
+    if constexpr (N >= 2) {
+        const bool upper = (c & M) != 0;
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+            const float send = upper ? x[j] : x[j + N / 2];
+            const float keep = upper ? x[j + N / 2] : x[j];
+            x[j] = keep + __shfl_xor_sync(FULL, send, M);
+        }
+    } else {
+        x[0] += __shfl_xor_sync(FULL, x[0], M);
+    }
+}
+
+// Max / sum over the 16 lanes that share lane bit 0 (xor 2, 4, 8, 16).
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int m = 2; m <= 16; m <<= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, m));
+    return v;
+}
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int m = 2; m <= 16; m <<= 1) v += __shfl_xor_sync(FULL, v, m);
+    return v;
+}
+
+template <int G>
+__global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
+{
+    constexpr int V = 8 * G;                 // partial dot products per lane per chunk
+    constexpr int R = V >= 16 ? V / 16 : 1;  // whole dot products per lane after the butterfly
+    const int b = blockIdx.x, s = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, c = lane & 15;
+
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) {
+        if (s == 0 && threadIdx.x == 0) pa::report(p.status, PA_ERR_BOUNDS);
+        ctx = 0;
+    }
+    if (ctx == 0) {  // padded row: output zeros, read nothing
+        if (s == 0) {
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.num_heads * D);
+            for (int i = threadIdx.x; i < p.num_heads * D / 8; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    const int nsplit = (ctx + p.split_len - 1) / p.split_len;
+    if (s >= nsplit) return;
+
+    const int g = warp % p.kv_heads;
+    const int sub = warp / p.kv_heads;
+    const int wph = NW / p.kv_heads;
+    const int t0 = s * p.split_len;
+    const int t1 = min(ctx, t0 + p.split_len);
+    const int64_t row_elems = int64_t(p.kv_heads) * D;
+
+    float qf[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + h) * D + 8 * c);
+        unpack8(u, qf[h]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
+    }
+    float o[G][8];
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+    }
+
+    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+    for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
+        const int32_t phys = table[cb / p.block_size];
+        if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+            if (lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            continue;
+        }
+        // a chunk never crosses a block: cb and block_size are multiples of 16
+        const int64_t row0 = int64_t(phys) * p.block_size + (cb % p.block_size) + half * 8;
+        const uint16_t *kp = p.k_cache + row0 * row_elems + g * D + 8 * c;
+        const uint16_t *vp = p.v_cache + row0 * row_elems + g * D + 8 * c;
+        const int nvalid = t1 - (cb + half * 8);  // tokens of this half inside the split
+
+        uint4 kr[8], vr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < nvalid) {
+                kr[i] = pa::ld_stream16(kp + i * row_elems);
+                vr[i] = pa::ld_stream16(vp + i * row_elems);
+            } else {
+                kr[i] = make_uint4(0, 0, 0, 0);
+                vr[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+
+        // partial dot products over this lane's 8 dims: x[i * G + h]
+        float x[8 * 8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float kf[8];
+            unpack8(kr[i], kf);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+                x[i * G + h] = acc;
+            }
+        }
+        xpose_step<V, 8>(x, c);
+        xpose_step<V / 2, 4>(x, c);
+        xpose_step<V / 4, 2>(x, c);
+        xpose_step<V / 8, 1>(x, c);
+        // lane c now holds token i = c >> 1 of its half; register r is head
+        // (c & 1) * R + r (G >= 2) or head 0 (G == 1).
+        const bool tok_ok = (c >> 1) < nvalid;
+        float sc[R], mx[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            sc[r] = tok_ok ? x[r] : -INFINITY;
+            mx[r] = group_max(sc[r]);
+        }
+        float m_new[G], alpha[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float mc = (G == 1) ? mx[0] : __shfl_sync(FULL, mx[h % R], h / R);
+            m_new[h] = fmaxf(m[h], mc);
+            alpha[h] = exp2f(m[h] - m_new[h]);
+        }
+        float pr[R], ps[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float mh = (G == 1) ? m_new[0] : ((c & 1) ? m_new[(R + r) % G] : m_new[r % G]);
+            pr[r] = exp2f(sc[r] - mh);
+            ps[r] = group_sum(pr[r]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float sum = (G == 1) ? ps[0] : __shfl_sync(FULL, ps[h % R], h / R);
+            l[h] = alpha[h] * l[h] + sum;
+            m[h] = m_new[h];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] *= alpha[h];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float vf[8];
+            unpack8(vr[i], vf);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const int idx = i * G + h;
+                const int src_c = (G == 1) ? 2 * i : idx / R;
+                const float pv = __shfl_sync(FULL, pr[(G == 1) ? 0 : idx % R], src_c, 16);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pv, vf[e], o[h][e]);
+            }
+        }
+    }
+
+    // the two halves saw different tokens of the same chunks: add them
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(FULL, o[h][e], 16);
+
+    // warps that shared one KV head (Hkv < 8) merge through shared memory
+    __shared__ float red_o[NW][G][D];
+    __shared__ float red_ml[NW][G][2];
+    if (wph > 1) {
+        if (lane < 16) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) red_o[warp][h][8 * c + e] = o[h][e];
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                red_ml[warp][h][0] = m[h];
+                red_ml[warp][h][1] = l[h];
+            }
+        }
+        __syncthreads();
+        if (sub != 0) return;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float mm = m[h];
+            for (int w = 1; w < wph; ++w) mm = fmaxf(mm, red_ml[g + w * p.kv_heads][h][0]);
+            const float a0 = exp2f(m[h] - mm);
+            float ll = l[h] * a0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] *= a0;
+            for (int w = 1; w < wph; ++w) {
+                const int ww = g + w * p.kv_heads;
+                const float mw = red_ml[ww][h][0];
+                const float aw = (mw == -INFINITY) ? 0.f : exp2f(mw - mm);
+                ll += red_ml[ww][h][1] * aw;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(red_o[ww][h][8 * c + e], aw, o[h][e]);
+            }
+            m[h] = mm;
+            l[h] = ll;
+        }
+    }
+
+    if (lane >= 16) return;
+    if (nsplit == 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float inv = 1.f / l[h];
+            uint4 u;
+            u.x = pa::pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
+            u.y = pa::pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
+            u.z = pa::pack_bf16x2(o[h][4] * inv, o[h][5] * inv);
+            u.w = pa::pack_bf16x2(o[h][6] * inv, o[h][7] * inv);
+            *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + g * G + h) * D + 8 * c) = u;
+        }
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const int64_t row = (int64_t(b) * p.max_splits + s) * p.num_heads + g * G + h;
+        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + row * D + 8 * c);
+        dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        if (c == 0) p.ws_ml[row] = make_float2(m[h], l[h]);
+    }
+}
+
+// Merge the split partials of every sequence that has more than one split
+// ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
+// L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
+{
+    const int b = blockIdx.x;
+    int ctx = p.context_lens[b];
+    if (ctx <= 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) return;
+    const int nsplit = (ctx + p.split_len - 1) / p.split_len;
+    if (nsplit <= 1) return;
+    for (int item = threadIdx.x; item < p.num_heads * (D / 8); item += blockDim.x) {
+        const int h = item / (D / 8), c = item % (D / 8);
+        const int64_t base = int64_t(b) * p.max_splits * p.num_heads + h;
+        float mm = -INFINITY;
+        for (int s = 0; s < nsplit; ++s) mm = fmaxf(mm, p.ws_ml[base + int64_t(s) * p.num_heads].x);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float ll = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const int64_t row = base + int64_t(s) * p.num_heads;
+            const float2 ml = p.ws_ml[row];
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mm);
+            ll += ml.y * w;
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * D + 8 * c);
+            const float4 a = src[0], bb = src[1];
+            acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
+            acc[4] += bb.x * w; acc[5] += bb.y * w; acc[6] += bb.z * w; acc[7] += bb.w * w;
+        }
+        const float inv = 1.f / ll;
+        uint4 u;
+        u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + h) * D + 8 * c) = u;
+    }
+}
+
+template <int G>
+void launch_split(const DecodeParams &p, cudaStream_t stream)
+{
+    const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
+    decode_split_kernel<G><<<grid, NW * 32, 0, stream>>>(p);
+}
+
+pa_status check_args(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
+                     int64_t num_blocks, int block_size, const int32_t *block_table, int max_blocks,
+                     const int32_t *context_lens, int num_seqs, int max_ctx, int num_heads, int kv_heads,
+                     int head_dim, const void *out)
+{
+    if (num_seqs < 0 || max_ctx < 0 || num_blocks < 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != D || !pa::pow2_in(kv_heads, 1, 8) || num_heads <= 0 || num_heads % kv_heads != 0 ||
+        !pa::pow2_in(num_heads / kv_heads, 1, 8))
+        return PA_ERR_UNSUPPORTED;
+    if (block_size < 16 || block_size > 1024 || block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (max_blocks < 1) return PA_ERR_INVALID_ARG;
+    if (q_stride_seq < int64_t(num_heads) * D || q_stride_seq % 8 != 0) return PA_ERR_INVALID_ARG;
+    if (!pa::aligned(q, 16) || !pa::aligned(k_cache, 16) || !pa::aligned(v_cache, 16) || !pa::aligned(out, 16))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len)
+{
+    if (num_seqs < 0 || num_heads <= 0 || head_dim != D || max_context_len < 0) return 0;
+    return workspace_bytes(num_seqs, num_heads, make_plan(num_seqs, max_context_len));
+}
+
+extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
+                                     int64_t num_blocks, int block_size, const int32_t *block_table,
+                                     int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                     int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                                     float scale, void *out, void *workspace, size_t workspace_bytes_given,
+                                     int32_t *dev_status, void *stream)
+{
+    pa_status st = check_args(q, q_stride_seq, k_cache, v_cache, num_blocks, block_size, block_table,
+                              max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
+                              num_kv_heads, head_dim, out);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const Plan plan = make_plan(num_seqs, max_context_len);
+    if (plan.max_splits > 65535) return PA_ERR_UNSUPPORTED;
+    const size_t need = workspace_bytes(num_seqs, num_heads, plan);
+    if (need > 0 && (workspace == nullptr || workspace_bytes_given < need || !pa::aligned(workspace, 256)))
+        return PA_ERR_INVALID_ARG;
+
+    DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_stride = q_stride_seq;
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.max_ctx = max_context_len;
+    p.num_heads = num_heads;
+    p.kv_heads = num_kv_heads;
+    p.scale_log2 = scale * LOG2E;
+    p.out = static_cast<uint16_t *>(out);
+    const size_t n = size_t(num_seqs) * (plan.max_splits > 0 ? plan.max_splits : 1) * num_heads;
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_ml = need > 0 ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                                   (n * D * sizeof(float) + 255) / 256 * 256)
+                       : nullptr;
+    p.split_len = plan.split_len;
+    p.max_splits = plan.max_splits;
+    p.status = dev_status;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (num_heads / num_kv_heads) {
+    case 1: launch_split<1>(p, s); break;
+    case 2: launch_split<2>(p, s); break;
+    case 4: launch_split<4>(p, s); break;
+    default: launch_split<8>(p, s); break;
+    }
+    if (plan.max_splits > 1) decode_merge_kernel<<<dim3(unsigned(num_seqs)), 256, 0, s>>>(p);
+    return pa::launch_status();
+}

@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads and exports every symbol include/pa.h
+declares; host-side argument checks reject bad calls before any CUDA work.
+No kernel is launched here (no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_110_gb300 import _build
+    _build.build()
+    from paged_kv_cache_110_gb300 import binding
+    return binding.lib
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("pa_store_kvcache", "pa_prefill_paged", "pa_decode_paged", "pa_decode_workspace_bytes",
+              "pa_status_string", "pa_kv_bytes_per_token", "pa_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from paged_kv_cache_110_gb300 import binding as pa
+    assert pa.pa_status_string(0) == "ok"
+    assert pa.pa_status_string(4) == "index out of bounds"
+    assert pa.pa_status_string(99) == "unknown status"
+    assert pa.pa_abi_version() >= 100
+
+
+def test_kv_bytes_closed_form(lib):
+    from paged_kv_cache_110_gb300 import binding as pa
+    assert pa.pa_kv_bytes_per_token(28, 8, 128, 2) == 114688
+    assert pa.pa_kv_bytes_per_token(28, 8, 128, 2) * 256 == 29360128
+    assert pa.pa_kv_bytes_per_token(0, 8, 128, 2) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null value; never dereferenced by the host checks below
+
+
+def test_store_host_checks(lib):
+    f = lib.pa_store_kvcache
+    ok = dict(k=FAKE, ks=1024, v=FAKE, vs=1024, n=4, hkv=8, d=128, kc=FAKE, vc=FAKE, nb=4, bs=16, slot=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["k"], a["ks"], a["v"], a["vs"], a["n"], a["hkv"], a["d"], a["kc"], a["vc"], a["nb"], a["bs"],
+                 a["slot"], None, None)
+
+    assert call(d=64) == 2
+    assert call(hkv=3) == 2
+    assert call(bs=24) == 2
+    assert call(n=-1) == 1
+    assert call(n=0) == 0          # nothing to do, nothing launched
+    assert call(k=None) == 1
+    assert call(slot=None) == 1
+    assert call(ks=512) == 1       # stride shorter than a row
+
+
+def test_prefill_host_checks(lib):
+    f = lib.pa_prefill_paged
+
+    def call(q=FAKE, qs=2048, k=None, v=None, kvs=0, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2, cuq=FAKE,
+             cuk=FAKE, ns=2, mq=8, mk=8, hq=16, hkv=8, d=128, out=FAKE):
+        return f(q, qs, k, v, kvs, kc, vc, nb, bs, bt, mb, cuq, cuk, ns, mq, mk, hq, hkv, d, ctypes.c_float(0.1),
+                 out, None, None)
+
+    assert call(d=64) == 2
+    assert call(hq=12, hkv=8) == 2
+    assert call(hq=32, hkv=2) == 2   # 16 query heads per KV head is not built
+    assert call(ns=0) == 0
+    assert call(mq=0) == 0
+    assert call(q=None) == 1
+    assert call(bt=None) == 1                               # no table and no k / v
+    assert call(bt=None, k=FAKE, v=FAKE, kvs=1024, mk=9) == 1  # null table needs max_seqlen_k == max_seqlen_q
+    assert call(qs=100) == 1
+
+
+def test_decode_host_checks(lib):
+    f = lib.pa_decode_paged
+
+    def call(q=FAKE, qs=2048, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2, ctx=FAKE, ns=2, mctx=32, hq=16,
+             hkv=8, d=128, out=FAKE, ws=None, wsb=0):
+        return f(q, qs, kc, vc, nb, bs, bt, mb, ctx, ns, mctx, hq, hkv, d, ctypes.c_float(0.1), out, ws, wsb,
+                 None, None)
+
+    assert call(d=256) == 2
+    assert call(hkv=16, hq=16) == 2
+    assert call(bs=8) == 2
+    assert call(ns=0) == 0
+    assert call(ns=-1) == 1
+    assert call(ctx=None) == 1
+    assert call(q=FAKE + 2) == 1   # q must be 16-byte aligned
