@@ -52,7 +52,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 # DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
 # valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha256": None, "bytes_per_call": None}
+NCU_TRAFFIC = {"source_sha256": "f1b8af4f9bd84c0ce98c0ef90dd4132dea8a05a981cce4fd992a1eb071e7c644",
+               "bytes_per_call": 586_690_304 + 5_865_216, "kernel": "decode_split_kernel<2>"}
 
 
 def _file_sha(path):
@@ -160,7 +161,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.05)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -171,10 +177,13 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Samples taken between host times t0 and t1 (the timed region)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -242,8 +251,6 @@ class DecodeStep:
                 events[-1][1].record()
 
     def launches_per_step(self):
-        splits = (self.max_ctx + 1) // 1  # placeholder, replaced below
-        del splits
         return self.layers * (1 + (2 if self._multi_split() else 1))
 
     def _multi_split(self):
@@ -451,11 +458,12 @@ def reference_arm(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -470,7 +478,8 @@ def main():
     device = torch.device("cuda", local)
     peaks, peak_kind = measured_peaks()
 
-    step = DecodeStep(device, seed=wl.SEED_BASE + 2 + 10000 * rank, keep_host_layer0=(rank == 0))
+    step = DecodeStep(device, seed=wl.SEED_BASE + 2 + 10000 * rank, layers=args.layers,
+                      keep_host_layer0=(rank == 0))
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -479,7 +488,11 @@ def main():
         os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
     events = []
     with ClockSampler(gpu_index) as clocks:
+        clocks.wait_first()
+        h0 = time.time()
         elapsed = time_region(lambda: step.run(events), args.steps, world)
+        h1 = time.time()
+        time.sleep(0.3)
     t_max, bytes_all = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
     value = bytes_all / t_max / 1e9
     decode_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
@@ -499,9 +512,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "decode batch x 28 layers: 256 seqs, context_lens U[100,1024], block_size 256, "
                                "16q/8kv x 128 bf16; per layer KV write of 256 tokens + paged decode",
-                   "layers": LAYERS, "seqs": step.B, "sum_context": int(step.ctx.sum()),
+                   "layers": step.layers, "seqs": step.B, "sum_context": int(step.ctx.sum()),
                    "l2": "inputs larger than L2: 28 distinct layer pools (%.1f GB)" %
-                         (LAYERS * 2 * step.layout.num_blocks * 256 * ROW_BYTES / 1e9),
+                         (step.layers * 2 * step.layout.num_blocks * 256 * ROW_BYTES / 1e9),
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": world * step.B * args.steps / t_max,
         "hbm_frac_of_8tbs": value / 8000.0,
@@ -511,9 +524,10 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "pa_decode_paged (split + merge kernels)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes_per_call": step.decode_bytes,
+                     "traffic": traffic, "traffic_kernel": NCU_TRAFFIC["kernel"],
+                     "algorithmic_bytes_per_call": step.decode_bytes,
                      "us_per_call": decode_s * 1e6},
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(h0, h1 + 0.25),
     }
     if rank == 0 and not args.no_extras:
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
