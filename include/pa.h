@@ -165,6 +165,40 @@ pa_status pa_decode_paged(const void *q, int64_t q_stride_seq,
                           int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * Paged decode for callers that cannot allocate device memory.  (The pages
+ * describe no counterpart: this is a calling convention of this library.)
+ *
+ * Who needs it: code embedded in a host framework that owns the whole device
+ * memory pool and forbids foreign cudaMalloc calls, services that must not
+ * allocate once they serve requests, and plain C callers with no
+ * device-memory manager.  Such callers cannot provide the workspace that
+ * pa_decode_paged asks for.
+ *
+ * Same arguments and result as pa_decode_paged, without the workspace: the
+ * split partials live in a fixed device array inside this library, of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES bytes, that every GPU which loads the
+ * library holds until the process exits.  The call allocates nothing.
+ *   - If pa_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ *     max_context_len) exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES, it returns
+ *     PA_ERR_UNSUPPORTED and launches nothing; use pa_decode_paged then.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and give wrong
+ *     results.  Calls on one stream are ordered and safe.  The array keeps
+ *     the last call's contents; nothing in it needs to start at zero.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+pa_status pa_decode_paged_noalloc(const void *q, int64_t q_stride_seq,
+                                  const void *k_cache, const void *v_cache, int64_t num_blocks, int block_size,
+                                  const int32_t *block_table, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int num_seqs, int max_context_len,
+                                  int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
+                                  int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,7 @@ from . import _build
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
     "pa_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+    "pa_decode_paged_noalloc",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
@@ -51,6 +52,9 @@ def _load() -> ctypes.CDLL:
     L.pa_decode_paged.restype = i32
     L.pa_decode_paged.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp,
                                   vp, sz, vp, vp]
+    L.pa_decode_paged_noalloc.restype = i32
+    L.pa_decode_paged_noalloc.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32,
+                                          vp, vp, vp]
     return L
 
 
@@ -179,3 +183,24 @@ def pa_decode_paged(q, k_cache, v_cache, block_table, context_lens, max_context_
                                float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                _stream(stream)),
            "pa_decode_paged")
+
+
+def pa_decode_paged_noalloc(q, k_cache, v_cache, block_table, context_lens, max_context_len, scale, out,
+                            dev_status=None, stream=None):
+    """Paged decode for callers that cannot allocate device memory: no
+    workspace argument; the library's fixed device scratch is used instead
+    (see include/pa.h).  Calls that overlap on the GPU must not be issued."""
+    hq, qs = _bf16_rows(q, "q")
+    nb, bs, hkv, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(block_table, "block_table")
+    _i32(context_lens, "context_lens")
+    b = q.shape[0]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (b, hq, d):
+        raise ValueError("out must be a contiguous bf16 [B, Hq, D] tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != b or context_lens.numel() != b:
+        raise ValueError("block_table / context_lens do not match q")
+    _check(lib.pa_decode_paged_noalloc(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table),
+                                       block_table.shape[1], _ptr(context_lens), b, int(max_context_len), hq, hkv,
+                                       d, float(scale), _ptr(out), _ptr(dev_status), _stream(stream)),
+           "pa_decode_paged_noalloc")

@@ -28,6 +28,7 @@
 //    a small merge kernel combines them; a single-split sequence is
 //    finalised in place.
 #include <cstdlib>
+#include <mutex>
 
 #include "pa_common.cuh"
 
@@ -468,4 +469,59 @@ extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const 
     }
     if (plan.max_splits > 1) decode_merge_kernel<<<dim3(unsigned(num_seqs)), 256, 0, s>>>(p);
     return pa::launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided scratch.
+//
+// Some callers cannot allocate device memory: code embedded in a host
+// framework that owns the whole device memory pool and forbids foreign
+// cudaMalloc calls, services that must not allocate once they are serving,
+// and plain C callers with no device-memory manager at all.  For them the
+// split partials live in this file-scope device array instead of a
+// workspace argument.  Every GPU that loads this library holds the array
+// until the process exits.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[PA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (in host code the array's name is
+// only a host-side stand-in, never a device address).
+pa_status noalloc_scratch_address(void **out)
+{
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_paged_noalloc(const void *q, int64_t q_stride_seq, const void *k_cache,
+                                             const void *v_cache, int64_t num_blocks, int block_size,
+                                             const int32_t *block_table, int max_blocks_per_seq,
+                                             const int32_t *context_lens, int num_seqs, int max_context_len,
+                                             int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
+                                             int32_t *dev_status, void *stream)
+{
+    if (num_seqs < 0 || max_context_len < 0 || num_heads <= 0 || head_dim != D) return PA_ERR_INVALID_ARG;
+    if (pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len) > PA_DECODE_NOALLOC_SCRATCH_BYTES)
+        return PA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const pa_status st = noalloc_scratch_address(&scratch);
+    if (st != PA_OK) return st;
+    // The kernels write every partial they later read within one call, so
+    // nothing in the scratch has to start at zero.
+    return pa_decode_paged(q, q_stride_seq, k_cache, v_cache, num_blocks, block_size, block_table,
+                           max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                           head_dim, scale, out, scratch, PA_DECODE_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }
