@@ -311,12 +311,15 @@ def flush_l2(buf):
     buf.add_(1)
 
 
-def time_prefill(device, steps, warmup, flush):
+def time_prefill(device, steps, warmup, flush, only="all"):
     from paged_kv_cache_110_gb300 import binding as pa
     res = {}
-    cases = {"varlen_16k": [wl.varlen_prefill(device=device)]}
-    a, b, _ = wl.prefix_chunk(device=device)
-    cases["prefix_2048_chunked"] = [a, b]
+    cases = {}
+    if only in ("all", "varlen_16k"):
+        cases["varlen_16k"] = [wl.varlen_prefill(device=device)]
+    if only in ("all", "prefix_2048_chunked"):
+        a, b, _ = wl.prefix_chunk(device=device)
+        cases["prefix_2048_chunked"] = [a, b]
     for name, calls in cases.items():
         kc, vc = calls[0].k_cache, calls[0].v_cache
         prepared = []
@@ -464,6 +467,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
+    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode"],
+                    help="run one secondary leg alone (profiling); prints that leg's results only")
+    ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -477,6 +483,15 @@ def main():
     __graft_entry__.build()
     device = torch.device("cuda", local)
     peaks, peak_kind = measured_peaks()
+    if args.leg != "all":
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        if args.leg == "prefill":
+            res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
+        else:
+            res = time_long_decode(device, max(args.steps, 1), args.warmup, flush)
+        if rank == 0:
+            print(json.dumps({"leg": args.leg, "results": res}), flush=True)
+        return 0
 
     step = DecodeStep(device, seed=wl.SEED_BASE + 2 + 10000 * rank, layers=args.layers,
                       keep_host_layer0=(rank == 0))

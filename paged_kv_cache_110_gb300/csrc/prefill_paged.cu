@@ -15,11 +15,16 @@
 //               height is gcd(block_size, 128) rows, so a box never crosses a
 //               page; without a table, rows are copied with cp.async.  All
 //               tiles land in shared memory in the 128-byte-swizzled layout
-//               the tensor cores read.  Two K/V stages.
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//               the tensor cores read.  Three K stages (a K tile is released
+//               as soon as its S is computed) and two V stages; K runs one
+//               tile ahead of V.
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of three TMEM
 //               S buffers (M = N = 128, K = 128 in eight K = 16 steps), and
 //               O += P_{j-1} V_{j-1} with P read from TMEM, so S_{j} is on the
-//               tensor cores while the softmax warps work on S_{j-1}.
+//               tensor cores while the softmax warps work on S_{j-1}.  An S
+//               buffer is reused only after the P.V that reads its P has
+//               completed (tensor-core reads and writes of one TMEM region
+//               by different MMAs are ordered explicitly).
 //   warps 4-7   softmax, one thread per query row: read the S row from TMEM,
 //               mask (causal, bottom-right, and keys past the tile's last
 //               visible key), base-2 exponentials with scale * log2(e) folded
@@ -45,29 +50,34 @@ using namespace pa::sm100;
 constexpr int D = pa::kHeadDim;
 constexpr int BM = 128;             // queries per CTA (TMEM lanes)
 constexpr int BN = 128;             // keys per tile
-constexpr int STAGES = 2;
+constexpr int KSTAGES = 3;          // K tiles in flight (released as soon as S = Q K^T is done)
+constexpr int VSTAGES = 2;          // V tiles in flight (released after O += P V)
+constexpr int SBUF = 3;             // TMEM S buffers (P is written back over S)
 constexpr int NTHREADS = 256;
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
 constexpr int TILE_BYTES = 2 * HALF_BYTES;  // 128 rows x 128 bf16
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE_BYTES;
-constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
-constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+constexpr int OFF_V = OFF_K + KSTAGES * TILE_BYTES;
+constexpr int OFF_BAR = OFF_V + VSTAGES * TILE_BYTES;
 enum {
     B_Q = 0,
     B_KF = 1,
-    B_VF = B_KF + STAGES,
-    B_KVE = B_VF + STAGES,
-    B_SF = B_KVE + STAGES,
-    B_PF = B_SF + 2,
-    B_OD = B_PF + 2,
-    B_DRAIN = B_OD + 1,
+    B_KE = B_KF + KSTAGES,
+    B_VF = B_KE + KSTAGES,
+    B_VE = B_VF + VSTAGES,
+    B_SF = B_VE + VSTAGES,
+    B_PF = B_SF + SBUF,
+    B_SFREE = B_PF + SBUF,
+    B_OD = B_SFREE + SBUF,
+    B_OFIN = B_OD + 1,
+    B_DRAIN = B_OFIN + 1,
     NBAR = B_DRAIN + 1
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 bytes
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+constexpr uint32_t COL_O = 384;     // S buffers at columns 0, 128, 256
 constexpr long long WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -102,6 +112,54 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk)  // byte offset i
     return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Issue the loads of one 128-key tile of K (is_v = false) or V into `dst`,
+// arriving on `bar`.  Paged: lane 0 issues one TMA box per page run (boxes
+// at or past kend are skipped, boxes on an invalid block id are skipped and
+// reported).  No table: the 32 lanes copy rows with cp.async (rows past kend
+// zero-filled) and then arrive.
+__device__ __forceinline__ void load_tile(const TcParams &p, bool is_v, int b, int g, int k0, int j0, int kend,
+                                          uint32_t dst, uint32_t bar, int lane, bool &bad)
+{
+    if (p.block_table != nullptr) {
+        if (lane == 0) {
+            const CUtensorMap *map = is_v ? &p.vmap : &p.kmap;
+            const int nbox = BN / p.box_rows;
+            const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+            uint32_t bytes = 0;
+            for (int bx = 0; bx < nbox; ++bx) {
+                const int kb = j0 + bx * p.box_rows;
+                if (kb >= kend) break;
+                const int32_t phys = table[kb / p.block_size];
+                if (phys < 0 || int64_t(phys) >= p.num_blocks) { bad = true; continue; }
+                bytes += uint32_t(p.box_rows) * 128u * 2u;
+            }
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int bx = 0; bx < nbox; ++bx) {
+                const int kb = j0 + bx * p.box_rows;
+                if (kb >= kend) break;
+                const int32_t phys = table[kb / p.block_size];
+                if (phys < 0 || int64_t(phys) >= p.num_blocks) continue;
+                const int y = int(int64_t(phys) * p.block_size + kb % p.block_size);
+                const uint32_t off = uint32_t(bx * p.box_rows * 128);
+                tma_load_2d(dst + off, map, g * D, y, bar);
+                tma_load_2d(dst + HALF_BYTES + off, map, g * D + 64, y, bar);
+            }
+        }
+        __syncwarp();
+    } else {
+        const uint16_t *base = is_v ? p.v : p.k;
+        for (int idx = lane; idx < BN * 16; idx += 32) {
+            const int r = idx >> 4, c = idx & 15;
+            const bool valid = j0 + r < kend;
+            const uint16_t *src = valid ? base + (int64_t(k0) + j0 + r) * p.kv_stride + g * D + c * 8 : p.q;
+            cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7), src, valid);
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(bar);
+    }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -133,17 +191,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const int ntiles = (kend + BN - 1) / BN;
 
     if (threadIdx.x == 0) {
+        const uint32_t loader_count = paged ? 1 : 32;
         mbar_init(bar(B_Q), 32);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(B_KF + s), paged ? 1 : 32);
-            mbar_init(bar(B_VF + s), paged ? 1 : 32);
-            mbar_init(bar(B_KVE + s), 1);
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(bar(B_KF + s), loader_count);
+            mbar_init(bar(B_KE + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(bar(B_VF + s), loader_count);
+            mbar_init(bar(B_VE + s), 1);
+        }
+        for (int s = 0; s < SBUF; ++s) {
             mbar_init(bar(B_SF + s), 1);
             mbar_init(bar(B_PF + s), 128);
+            mbar_init(bar(B_SFREE + s), 1);
         }
         mbar_init(bar(B_OD), 1);
+        mbar_init(bar(B_OFIN), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -159,11 +223,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        bool bad = false;
+        // order: K_0, Q, then K_{j+1} ahead of V_j, so S = Q K^T can start as
+        // soon as possible and V trails by one tile
+        bool bad = false, ok = true;
         if (paged && lane == 0) {
             tma_prefetch_desc(&p.kmap);
             tma_prefetch_desc(&p.vmap);
         }
+        load_tile(p, false, b, g, k0, 0, kend, sb + OFF_K, bar(B_KF), lane, bad);
         for (int idx = lane; idx < BM * 16; idx += 32) {
             const int r = idx >> 4, c = idx & 15;
             const bool valid = r < rows;
@@ -173,67 +240,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(bar(B_Q));
-
-        int issued_upto = 0;  // tiles whose loads were issued
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j % STAGES;
-            if (j >= STAGES && !mbar_wait(bar(B_KVE + st), ((j / STAGES) - 1) & 1, abort_flag, WAIT_LIMIT)) break;
-            const int j0 = j * BN;
-            const uint32_t kdst = sb + OFF_K + st * TILE_BYTES, vdst = sb + OFF_V + st * TILE_BYTES;
-            if (paged) {
-                if (lane == 0) {
-                    const int nbox = BN / p.box_rows;
-                    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
-                    uint32_t bytes = 0;
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        const int kb = j0 + bx * p.box_rows;
-                        if (kb >= kend) break;
-                        const int32_t phys = table[kb / p.block_size];
-                        if (phys < 0 || int64_t(phys) >= p.num_blocks) { bad = true; continue; }
-                        bytes += uint32_t(p.box_rows) * 128u * 2u;
-                    }
-                    mbar_arrive_expect_tx(bar(B_KF + st), bytes);
-                    mbar_arrive_expect_tx(bar(B_VF + st), bytes);
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        const int kb = j0 + bx * p.box_rows;
-                        if (kb >= kend) break;
-                        const int32_t phys = table[kb / p.block_size];
-                        if (phys < 0 || int64_t(phys) >= p.num_blocks) continue;
-                        const int y = int(int64_t(phys) * p.block_size + kb % p.block_size);
-                        const uint32_t off = uint32_t(bx * p.box_rows * 128);
-                        for (int hf = 0; hf < 2; ++hf) {
-                            tma_load_2d(kdst + hf * HALF_BYTES + off, &p.kmap, g * D + hf * 64, y, bar(B_KF + st));
-                            tma_load_2d(vdst + hf * HALF_BYTES + off, &p.vmap, g * D + hf * 64, y, bar(B_VF + st));
-                        }
-                    }
-                }
-                __syncwarp();
-            } else {
-                for (int idx = lane; idx < BN * 16; idx += 32) {
-                    const int r = idx >> 4, c = idx & 15;
-                    const bool valid = j0 + r < kend;
-                    const int64_t row = int64_t(k0) + j0 + r;
-                    const uint16_t *ks = valid ? p.k + row * p.kv_stride + g * D + c * 8 : p.q;
-                    const uint16_t *vs = valid ? p.v + row * p.kv_stride + g * D + c * 8 : p.q;
-                    const uint32_t o = (c >> 3) * HALF_BYTES + swz128(r, c & 7);
-                    cp_async16(kdst + o, ks, valid);
-                    cp_async16(vdst + o, vs, valid);
-                }
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                mbar_arrive(bar(B_KF + st));
-                mbar_arrive(bar(B_VF + st));
+        int k_issued = 1, v_issued = 0;
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const int jk = j + 1;  // K tile to issue in this round
+            if (jk < ntiles) {
+                const int st = jk % KSTAGES;
+                if (jk >= KSTAGES && !(ok = mbar_wait(bar(B_KE + st), ((jk / KSTAGES) - 1) & 1, abort_flag, WAIT_LIMIT)))
+                    break;
+                load_tile(p, false, b, g, k0, jk * BN, kend, sb + OFF_K + st * TILE_BYTES, bar(B_KF + st), lane, bad);
+                k_issued = jk + 1;
             }
-            issued_upto = j + 1;
+            const int sv = j % VSTAGES;
+            if (j >= VSTAGES && !(ok = mbar_wait(bar(B_VE + sv), ((j / VSTAGES) - 1) & 1, abort_flag, WAIT_LIMIT)))
+                break;
+            load_tile(p, true, b, g, k0, j * BN, kend, sb + OFF_V + sv * TILE_BYTES, bar(B_VF + sv), lane, bad);
+            v_issued = j + 1;
         }
         if (bad && lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
         if (*abort_flag && paged && lane == 0) {
             // let copies already in flight land before the CTA's shared memory goes away
-            for (int j = max(0, issued_upto - STAGES); j < issued_upto; ++j) {
-                volatile int32_t dummy = 0;
-                mbar_wait(bar(B_KF + j % STAGES), (j / STAGES) & 1, &dummy, WAIT_LIMIT);
-                mbar_wait(bar(B_VF + j % STAGES), (j / STAGES) & 1, &dummy, WAIT_LIMIT);
-            }
+            volatile int32_t dummy = 0;
+            for (int j = max(0, k_issued - KSTAGES); j < k_issued; ++j)
+                mbar_wait(bar(B_KF + j % KSTAGES), (j / KSTAGES) & 1, &dummy, WAIT_LIMIT);
+            for (int j = max(0, v_issued - VSTAGES); j < v_issued; ++j)
+                mbar_wait(bar(B_VF + j % VSTAGES), (j / VSTAGES) & 1, &dummy, WAIT_LIMIT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -244,10 +274,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             tc_fence_after();
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
-                    const int st = j % STAGES;
-                    if (!(ok = mbar_wait(bar(B_KF + st), (j / STAGES) & 1, abort_flag, WAIT_LIMIT))) break;
+                    const int st = j % KSTAGES, sbuf = j % SBUF;
+                    if (!(ok = mbar_wait(bar(B_KF + st), (j / KSTAGES) & 1, abort_flag, WAIT_LIMIT))) break;
+                    // the S buffer still holds P of tile j - SBUF until that tile's P.V has completed
+                    if (j >= SBUF &&
+                        !(ok = mbar_wait(bar(B_SFREE + sbuf), ((j / SBUF) - 1) & 1, abort_flag, WAIT_LIMIT)))
+                        break;
                     tc_fence_after();
-                    const uint32_t d = tmem + ((j & 1) ? COL_S1 : COL_S0);
+                    const uint32_t d = tmem + uint32_t(sbuf) * 128u;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
@@ -255,21 +289,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                         const uint64_t bk = smem_desc(sb + OFF_K + st * TILE_BYTES + hf * HALF_BYTES + ko, 16, 1024);
                         mma_ss(d, a, bk, IDESC_QK, kk > 0);
                     }
-                    mma_commit(bar(B_SF + (j & 1)));
+                    mma_commit(bar(B_SF + sbuf));
+                    mma_commit(bar(B_KE + st));
                 }
                 if (j >= 1) {
-                    const int jp = j - 1, sp = jp % STAGES;
-                    if (!(ok = mbar_wait(bar(B_PF + (jp & 1)), (jp >> 1) & 1, abort_flag, WAIT_LIMIT))) break;
-                    if (!(ok = mbar_wait(bar(B_VF + sp), (jp / STAGES) & 1, abort_flag, WAIT_LIMIT))) break;
+                    const int jp = j - 1, sv = jp % VSTAGES, pbuf = jp % SBUF;
+                    if (!(ok = mbar_wait(bar(B_PF + pbuf), (jp / SBUF) & 1, abort_flag, WAIT_LIMIT))) break;
+                    if (!(ok = mbar_wait(bar(B_VF + sv), (jp / VSTAGES) & 1, abort_flag, WAIT_LIMIT))) break;
                     tc_fence_after();
-                    const uint32_t pcol = tmem + ((jp & 1) ? COL_S1 : COL_S0);
+                    const uint32_t pcol = tmem + uint32_t(pbuf) * 128u;
 #pragma unroll
                     for (int s = 0; s < BN / 16; ++s) {
-                        const uint64_t bv = smem_desc(sb + OFF_V + sp * TILE_BYTES + s * 2048, HALF_BYTES, 1024);
+                        const uint64_t bv = smem_desc(sb + OFF_V + sv * TILE_BYTES + s * 2048, HALF_BYTES, 1024);
                         mma_ts(tmem + COL_O, pcol + s * 8, bv, IDESC_PV, (jp > 0 || s > 0) ? 1u : 0u);
                     }
-                    mma_commit(bar(B_KVE + sp));
+                    mma_commit(bar(B_VE + sv));
+                    mma_commit(bar(B_SFREE + pbuf));
                     mma_commit(bar(B_OD));
+                    if (jp == ntiles - 1) mma_commit(bar(B_OFIN));
                 }
             }
             if (!ok) {
@@ -287,34 +324,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         const uint32_t lane_base = uint32_t(quarter * 32) << 16;
         const int pos = offset + m0 + r;
         const int last_visible = min(pos, kend - 1);
-        float m_used = -INFINITY, l = 0.f;
+        const float sl2 = p.scale_log2;
+        float m_used = -INFINITY;  // running max in scaled base-2 units
+        float l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            ok = __all_sync(FULL, mbar_wait(bar(B_SF + (j & 1)), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
+            const int sbuf = j % SBUF;
+            ok = __all_sync(FULL, mbar_wait(bar(B_SF + sbuf), (j / SBUF) & 1, abort_flag, WAIT_LIMIT));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t scol = tmem + lane_base + ((j & 1) ? COL_S1 : COL_S0);
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(scol + cc * 32, sr[cc]);
-            tmem_ld_wait();
+            const uint32_t scol = tmem + lane_base + uint32_t(sbuf) * 128u;
+            uint32_t sr[128];
+            tmem_ld128_sync(scol, sr);
             const int j0 = j * BN;
-            const bool mask = j0 + BN - 1 > offset + m0;
-            const int limit = last_visible - j0;
-            float mx = -INFINITY;
+            if (j0 + BN - 1 > offset + m0) {  // the tile crosses some row's causal bound
+                const int limit = last_visible - j0;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float s = __uint_as_float(sr[cc][i]) * p.scale_log2;
-                    if (mask && cc * 32 + i > limit) s = -INFINITY;
-                    sr[cc][i] = __float_as_uint(s);
-                    mx = fmaxf(mx, s);
-                }
+                for (int c = 0; c < 128; ++c)
+                    if (c > limit) sr[c] = 0xff800000u;  // -inf
             }
+            // raw row max with 8 independent three-input max chains
+            float mx8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
+#pragma unroll
+            for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmax3(mx8[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+            }
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
             const bool need = mx > m_used + RESCALE_THRESHOLD;
             const float m_new = need ? mx : m_used;
-            const float factor = need ? exp2f(m_used - m_new) : 1.f;
+            const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
             if (j > 0 && __any_sync(FULL, need)) {
                 ok = __all_sync(FULL, mbar_wait(bar(B_OD), (j - 1) & 1, abort_flag, WAIT_LIMIT));
                 if (!ok) break;
@@ -322,50 +364,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + COL_O + cc * 32, o);
-                    tmem_ld_wait();
+                    tmem_ld32_sync(tmem + lane_base + COL_O + cc * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-                    tmem_st32(tmem + lane_base + COL_O + cc * 32, o);
+                    tmem_st32_sync(tmem + lane_base + COL_O + cc * 32, o);
                 }
-                tmem_st_wait();
             }
             l *= factor;
             m_used = m_new;
-            const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-            float rs = 0.f;
+            const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
+            // p = 2^(s * scale * log2 e - m): paired FMAs, MUFU exponentials, paired sums
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[64];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c0 = hf * 64 + 2 * i;
-                    const float p0 = exp2f(__uint_as_float(sr[c0 >> 5][c0 & 31]) - msub);
-                    const float p1 = exp2f(__uint_as_float(sr[(c0 + 1) >> 5][(c0 + 1) & 31]) - msub);
-                    rs += p0 + p1;
-                    pk[i] = pa::pack_bf16x2(p0, p1);
-                }
-                tmem_st32(scol + hf * 32, pk);
+            for (int i = 0; i < 64; ++i) {
+                float x0, x1;
+                ffma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, nm, nm);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                fadd2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
+                pk[i] = pa::pack_bf16x2(p0, p1);
             }
-            l += rs;
+            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             if (paged && j == ntiles - 1 && kend < j0 + BN) {
                 // rows past the last visible key may be unused pool slots (any bits): make them 0
                 // so that 0 * V stays 0 in P.V
-                const int st = j % STAGES;
-                if (!(ok = mbar_wait(bar(B_VF + st), (j / STAGES) & 1, abort_flag, WAIT_LIMIT))) break;
+                const int sv = j % VSTAGES;
+                ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), (j / VSTAGES) & 1, abort_flag, WAIT_LIMIT));
+                if (!ok) break;
                 if (j0 + r >= kend) {
-                    uint4 *row0 = reinterpret_cast<uint4 *>(smem + OFF_V + st * TILE_BYTES + r * 128);
-                    uint4 *row1 = reinterpret_cast<uint4 *>(smem + OFF_V + st * TILE_BYTES + HALF_BYTES + r * 128);
+                    uint4 *row0 = reinterpret_cast<uint4 *>(smem + OFF_V + sv * TILE_BYTES + r * 128);
+                    uint4 *row1 = reinterpret_cast<uint4 *>(smem + OFF_V + sv * TILE_BYTES + HALF_BYTES + r * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) row0[c] = row1[c] = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
             }
-            tmem_st_wait();
+            tmem_st64_sync(scol, pk);
             tc_fence_before();
-            mbar_arrive(bar(B_PF + (j & 1)));
+            mbar_arrive(bar(B_PF + sbuf));
         }
-        if (ok) ok = __all_sync(FULL, mbar_wait(bar(B_OD), (ntiles - 1) & 1, abort_flag, WAIT_LIMIT));
+        // The final O waits on its own single-use barrier.  B_OD completes once
+        // per P.V, and when the epilogue arrives the last two P.V may both be
+        // in flight, so a parity wait on B_OD could alias an older phase.
+        // (The rescale waits on B_OD above are safe: the S_j commit they follow
+        // implies every earlier MMA, so B_OD is at most one phase behind.)
+        if (ok) ok = __all_sync(FULL, mbar_wait(bar(B_OFIN), 0, abort_flag, WAIT_LIMIT));
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
@@ -373,8 +416,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + COL_O + cc * 32, o);
-                tmem_ld_wait();
+                tmem_ld32_sync(tmem + lane_base + COL_O + cc * 32, o);
                 if (r < rows) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
 #pragma unroll
