@@ -10,8 +10,7 @@
 // running max, a running sum and an unnormalised numerator (§13.3).
 //
 // One CTA computes a 128-query tile of one (sequence, query head):
-//   warp 0      producer: the Q tile (cp.async) and, per 128-key tile, K and
-//               V.  Paged keys arrive by TMA, one box per page run: the box
+//   warps 0, 2  producers: warp 0 the Q tile (cp.async) and K, warp 2 V.  Paged keys arrive by TMA, one box per page run: the box
 //               height is gcd(block_size, 128) rows, so a box never crosses a
 //               page; without a table, rows are copied with cp.async.  All
 //               tiles land in shared memory in the 128-byte-swizzled layout
@@ -75,7 +74,9 @@ enum {
     NBAR = B_DRAIN + 1
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 bytes
+constexpr int TABLE_SMEM = 2048;                  // block-table entries staged in shared memory
+constexpr int OFF_TABLE = OFF_MISC + 16;
+constexpr int SMEM_BYTES = OFF_TABLE + TABLE_SMEM * 4 + 1024;  // + slack to align the base to 1024 bytes
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 384;     // S buffers at columns 0, 128, 256
 constexpr long long WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
@@ -112,47 +113,55 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk)  // byte offset i
     return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// Issue the loads of one 128-key tile of K (is_v = false) or V into `dst`,
-// arriving on `bar`.  Paged: lane 0 issues one TMA box per page run (boxes
-// at or past kend are skipped, boxes on an invalid block id are skipped and
-// reported).  No table: the 32 lanes copy rows with cp.async (rows past kend
-// zero-filled) and then arrive.
-__device__ __forceinline__ void load_tile(const TcParams &p, bool is_v, int b, int g, int k0, int j0, int kend,
-                                          uint32_t dst, uint32_t bar, int lane, bool &bad)
+// Where one producer warp reads a tile from: the TMA map of the paged pool
+// (with the sequence's block ids, staged in shared memory when they fit; -1
+// marks an id that failed validation), or the new-token rows when there is
+// no table.
+struct TileSource {
+    const CUtensorMap *map;  // paged
+    const int32_t *table;    // paged
+    int box_rows;
+    int block_size;
+    const uint16_t *rows;    // no table: first row of the sequence, head g
+    int64_t stride;          // no table: row stride in elements
+    const uint16_t *dummy;   // any mapped address (zero-byte cp.async source)
+};
+
+// Issue the loads of the 128-key tile starting at key j0 into `dst`,
+// arriving on `bar`.  Paged: lane 0 issues one TMA box per page run; boxes
+// at or past kend and boxes on invalid ids are skipped.  No table: the 32
+// lanes copy rows with cp.async (rows past kend zero-filled) and then arrive.
+__device__ __forceinline__ void load_tile(const TileSource &src, int xcol, int j0, int kend, uint32_t dst,
+                                          uint32_t bar, int lane)
 {
-    if (p.block_table != nullptr) {
+    if (src.map != nullptr) {
         if (lane == 0) {
-            const CUtensorMap *map = is_v ? &p.vmap : &p.kmap;
-            const int nbox = BN / p.box_rows;
-            const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+            const int nbox = BN / src.box_rows;
             uint32_t bytes = 0;
             for (int bx = 0; bx < nbox; ++bx) {
-                const int kb = j0 + bx * p.box_rows;
+                const int kb = j0 + bx * src.box_rows;
                 if (kb >= kend) break;
-                const int32_t phys = table[kb / p.block_size];
-                if (phys < 0 || int64_t(phys) >= p.num_blocks) { bad = true; continue; }
-                bytes += uint32_t(p.box_rows) * 128u * 2u;
+                if (src.table[kb / src.block_size] >= 0) bytes += uint32_t(src.box_rows) * 128u * 2u;
             }
             mbar_arrive_expect_tx(bar, bytes);
             for (int bx = 0; bx < nbox; ++bx) {
-                const int kb = j0 + bx * p.box_rows;
+                const int kb = j0 + bx * src.box_rows;
                 if (kb >= kend) break;
-                const int32_t phys = table[kb / p.block_size];
-                if (phys < 0 || int64_t(phys) >= p.num_blocks) continue;
-                const int y = int(int64_t(phys) * p.block_size + kb % p.block_size);
-                const uint32_t off = uint32_t(bx * p.box_rows * 128);
-                tma_load_2d(dst + off, map, g * D, y, bar);
-                tma_load_2d(dst + HALF_BYTES + off, map, g * D + 64, y, bar);
+                const int32_t phys = src.table[kb / src.block_size];
+                if (phys < 0) continue;
+                const int y = int(int64_t(phys) * src.block_size + kb % src.block_size);
+                const uint32_t off = uint32_t(bx * src.box_rows * 128);
+                tma_load_2d(dst + off, src.map, xcol, y, bar);
+                tma_load_2d(dst + HALF_BYTES + off, src.map, xcol + 64, y, bar);
             }
         }
         __syncwarp();
     } else {
-        const uint16_t *base = is_v ? p.v : p.k;
         for (int idx = lane; idx < BN * 16; idx += 32) {
             const int r = idx >> 4, c = idx & 15;
             const bool valid = j0 + r < kend;
-            const uint16_t *src = valid ? base + (int64_t(k0) + j0 + r) * p.kv_stride + g * D + c * 8 : p.q;
-            cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7), src, valid);
+            const uint16_t *ptr = valid ? src.rows + int64_t(j0 + r) * src.stride + c * 8 : src.dummy;
+            cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7), ptr, valid);
         }
         cp_async_wait_all();
         fence_proxy_async_smem();
@@ -216,54 +225,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
         tmem_relinquish();
     }
+    // Stage the sequence's block ids (validated) in shared memory, so that
+    // issuing a tile never waits on a global load.
+    const int nblk = paged ? (kend + p.block_size - 1) / p.block_size : 0;
+    const bool table_in_smem = paged && nblk <= TABLE_SMEM;
+    if (paged && (warp == 2 || warp == 3)) {
+        const int32_t *gtable = p.block_table + int64_t(b) * p.max_blocks;
+        int32_t *st = reinterpret_cast<int32_t *>(smem + OFF_TABLE);
+        bool bad = false;
+        for (int i = threadIdx.x - 64; i < nblk; i += 64) {
+            int32_t phys = gtable[i];
+            if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+                bad = true;
+                phys = -1;
+            }
+            if (table_in_smem) st[i] = phys;
+        }
+        if (bad) pa::report(p.status, PA_ERR_BOUNDS);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        // order: K_0, Q, then K_{j+1} ahead of V_j, so S = Q K^T can start as
-        // soon as possible and V trails by one tile
-        bool bad = false, ok = true;
-        if (paged && lane == 0) {
-            tma_prefetch_desc(&p.kmap);
-            tma_prefetch_desc(&p.vmap);
-        }
-        load_tile(p, false, b, g, k0, 0, kend, sb + OFF_K, bar(B_KF), lane, bad);
-        for (int idx = lane; idx < BM * 16; idx += 32) {
-            const int r = idx >> 4, c = idx & 15;
-            const bool valid = r < rows;
-            const uint16_t *src = valid ? p.q + int64_t(q0 + m0 + r) * p.q_stride + h * D + c * 8 : p.q;
-            cp_async16(sb + OFF_Q + (c >> 3) * HALF_BYTES + swz128(r, c & 7), src, valid);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(bar(B_Q));
-        int k_issued = 1, v_issued = 0;
-        for (int j = 0; ok && j < ntiles; ++j) {
-            const int jk = j + 1;  // K tile to issue in this round
-            if (jk < ntiles) {
-                const int st = jk % KSTAGES;
-                if (jk >= KSTAGES && !(ok = mbar_wait(bar(B_KE + st), ((jk / KSTAGES) - 1) & 1, abort_flag, WAIT_LIMIT)))
-                    break;
-                load_tile(p, false, b, g, k0, jk * BN, kend, sb + OFF_K + st * TILE_BYTES, bar(B_KF + st), lane, bad);
-                k_issued = jk + 1;
+    TileSource src;
+    src.table = table_in_smem ? reinterpret_cast<const int32_t *>(smem + OFF_TABLE)
+                              : (paged ? p.block_table + int64_t(b) * p.max_blocks : nullptr);
+    src.box_rows = p.box_rows;
+    src.block_size = p.block_size;
+    src.stride = p.kv_stride;
+    src.dummy = p.q;
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
+        // warp 0: K_0, then Q, then K_1.. (a K stage is reused once the S that
+        // read it is done); warp 2: V_0, V_1.. (a V stage is reused once the
+        // P.V that read it is done).  Two warps, so K and V issue overlap.
+        const bool is_k = warp == 0;
+        src.map = paged ? (is_k ? &p.kmap : &p.vmap) : nullptr;
+        src.rows = paged ? nullptr : (is_k ? p.k : p.v) + int64_t(k0) * p.kv_stride + g * D;
+        if (paged && lane == 0) tma_prefetch_desc(src.map);
+        const int nst = is_k ? KSTAGES : VSTAGES;
+        const uint32_t base = sb + (is_k ? OFF_K : OFF_V);
+        const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_KE : B_VE;
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j % nst;
+            if (j >= nst && !(ok = mbar_wait(bar(empty0 + st), ((j / nst) - 1) & 1, abort_flag, WAIT_LIMIT))) break;
+            load_tile(src, g * D, j * BN, kend, base + st * TILE_BYTES, bar(full0 + st), lane);
+            issued = j + 1;
+            if (is_k && j == 0) {
+                for (int idx = lane; idx < BM * 16; idx += 32) {
+                    const int r = idx >> 4, c = idx & 15;
+                    const bool valid = r < rows;
+                    const uint16_t *qp = valid ? p.q + int64_t(q0 + m0 + r) * p.q_stride + h * D + c * 8 : p.q;
+                    cp_async16(sb + OFF_Q + (c >> 3) * HALF_BYTES + swz128(r, c & 7), qp, valid);
+                }
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_Q));
             }
-            const int sv = j % VSTAGES;
-            if (j >= VSTAGES && !(ok = mbar_wait(bar(B_VE + sv), ((j / VSTAGES) - 1) & 1, abort_flag, WAIT_LIMIT)))
-                break;
-            load_tile(p, true, b, g, k0, j * BN, kend, sb + OFF_V + sv * TILE_BYTES, bar(B_VF + sv), lane, bad);
-            v_issued = j + 1;
         }
-        if (bad && lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
+        (void)ok;
         if (*abort_flag && paged && lane == 0) {
             // let copies already in flight land before the CTA's shared memory goes away
             volatile int32_t dummy = 0;
-            for (int j = max(0, k_issued - KSTAGES); j < k_issued; ++j)
-                mbar_wait(bar(B_KF + j % KSTAGES), (j / KSTAGES) & 1, &dummy, WAIT_LIMIT);
-            for (int j = max(0, v_issued - VSTAGES); j < v_issued; ++j)
-                mbar_wait(bar(B_VF + j % VSTAGES), (j / VSTAGES) & 1, &dummy, WAIT_LIMIT);
+            for (int j = max(0, issued - nst); j < issued; ++j)
+                mbar_wait(bar(full0 + j % nst), (j / nst) & 1, &dummy, WAIT_LIMIT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
