@@ -19,11 +19,11 @@
 //               tile ahead of V.
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of three TMEM
 //               S buffers (M = N = 128, K = 128 in eight K = 16 steps), and
-//               O += P_{j-1} V_{j-1} with P read from TMEM, so S_{j} is on the
-//               tensor cores while the softmax warps work on S_{j-1}.  An S
-//               buffer is reused only after the P.V that reads its P has
-//               completed (tensor-core reads and writes of one TMEM region
-//               by different MMAs are ordered explicitly).
+//               O += P_j V_j with P read from TMEM, issued from a polling
+//               loop so S runs up to three tiles ahead of P.V.  An S buffer
+//               is reused only after the P.V that reads its P has completed
+//               (tensor-core reads and writes of one TMEM region by
+//               different MMAs are ordered explicitly).
 //   warps 4-7   softmax, one thread per query row: read the S row from TMEM,
 //               mask (causal, bottom-right, and keys past the tile's last
 //               visible key), base-2 exponentials with scale * log2(e) folded
@@ -49,8 +49,8 @@ using namespace pa::sm100;
 constexpr int D = pa::kHeadDim;
 constexpr int BM = 128;             // queries per CTA (TMEM lanes)
 constexpr int BN = 128;             // keys per tile
-constexpr int KSTAGES = 3;          // K tiles in flight (released as soon as S = Q K^T is done)
-constexpr int VSTAGES = 2;          // V tiles in flight (released after O += P V)
+constexpr int KSTAGES = 2;          // K tiles in flight (released as soon as S = Q K^T is done)
+constexpr int VSTAGES = 3;          // V tiles in flight (released after O += P V, so kept longer)
 constexpr int SBUF = 3;             // TMEM S buffers (P is written back over S)
 constexpr int NTHREADS = 256;
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
@@ -68,8 +68,7 @@ enum {
     B_SF = B_VE + VSTAGES,
     B_PF = B_SF + SBUF,
     B_SFREE = B_PF + SBUF,
-    B_OD = B_SFREE + SBUF,
-    B_OFIN = B_OD + 1,
+    B_OFIN = B_SFREE + SBUF,
     B_DRAIN = B_OFIN + 1,
     NBAR = B_DRAIN + 1
 };
@@ -215,7 +214,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             mbar_init(bar(B_PF + s), 128);
             mbar_init(bar(B_SFREE + s), 1);
         }
-        mbar_init(bar(B_OD), 1);
         mbar_init(bar(B_OFIN), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -295,46 +293,61 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // A polling state machine: S_j is issued as soon as K_j is in and its
+        // TMEM buffer is free (the P.V of tile j - SBUF has completed), and
+        // P.V_j as soon as P_j and V_j are in, so S runs up to SBUF tiles ahead
+        // of P.V and a late V tile does not hold back the softmax.
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
             bool ok = mbar_wait(bar(B_Q), 0, abort_flag, WAIT_LIMIT);
-            tc_fence_after();
-            for (int j = 0; ok && j <= ntiles; ++j) {
-                if (j < ntiles) {
-                    const int st = j % KSTAGES, sbuf = j % SBUF;
-                    if (!(ok = mbar_wait(bar(B_KF + st), (j / KSTAGES) & 1, abort_flag, WAIT_LIMIT))) break;
-                    // the S buffer still holds P of tile j - SBUF until that tile's P.V has completed
-                    if (j >= SBUF &&
-                        !(ok = mbar_wait(bar(B_SFREE + sbuf), ((j / SBUF) - 1) & 1, abort_flag, WAIT_LIMIT)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t d = tmem + uint32_t(sbuf) * 128u;
+            int ns = 0, npv = 0;  // next S tile, next P.V tile
+            long long t0 = clock64();
+            while (ok && npv < ntiles) {
+                bool progressed = false;
+                if (ns < ntiles && ns - npv < SBUF) {
+                    const int st = ns % KSTAGES, sbuf = ns % SBUF;
+                    if (mbar_poll(bar(B_KF + st), (ns / KSTAGES) & 1) &&
+                        (ns < SBUF || mbar_poll(bar(B_SFREE + sbuf), ((ns / SBUF) - 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t d = tmem + uint32_t(sbuf) * 128u;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
-                        const uint64_t a = smem_desc(sb + OFF_Q + hf * HALF_BYTES + ko, 16, 1024);
-                        const uint64_t bk = smem_desc(sb + OFF_K + st * TILE_BYTES + hf * HALF_BYTES + ko, 16, 1024);
-                        mma_ss(d, a, bk, IDESC_QK, kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
+                            const uint64_t a = smem_desc(sb + OFF_Q + hf * HALF_BYTES + ko, 16, 1024);
+                            const uint64_t bk = smem_desc(sb + OFF_K + st * TILE_BYTES + hf * HALF_BYTES + ko, 16, 1024);
+                            mma_ss(d, a, bk, IDESC_QK, kk > 0);
+                        }
+                        mma_commit(bar(B_SF + sbuf));
+                        mma_commit(bar(B_KE + st));
+                        ++ns;
+                        progressed = true;
                     }
-                    mma_commit(bar(B_SF + sbuf));
-                    mma_commit(bar(B_KE + st));
                 }
-                if (j >= 1) {
-                    const int jp = j - 1, sv = jp % VSTAGES, pbuf = jp % SBUF;
-                    if (!(ok = mbar_wait(bar(B_PF + pbuf), (jp / SBUF) & 1, abort_flag, WAIT_LIMIT))) break;
-                    if (!(ok = mbar_wait(bar(B_VF + sv), (jp / VSTAGES) & 1, abort_flag, WAIT_LIMIT))) break;
-                    tc_fence_after();
-                    const uint32_t pcol = tmem + uint32_t(pbuf) * 128u;
+                if (npv < ns) {
+                    const int sv = npv % VSTAGES, pbuf = npv % SBUF;
+                    if (mbar_poll(bar(B_PF + pbuf), (npv / SBUF) & 1) && mbar_poll(bar(B_VF + sv), (npv / VSTAGES) & 1)) {
+                        tc_fence_after();
+                        const uint32_t pcol = tmem + uint32_t(pbuf) * 128u;
 #pragma unroll
-                    for (int s = 0; s < BN / 16; ++s) {
-                        const uint64_t bv = smem_desc(sb + OFF_V + sv * TILE_BYTES + s * 2048, HALF_BYTES, 1024);
-                        mma_ts(tmem + COL_O, pcol + s * 8, bv, IDESC_PV, (jp > 0 || s > 0) ? 1u : 0u);
+                        for (int s = 0; s < BN / 16; ++s) {
+                            const uint64_t bv = smem_desc(sb + OFF_V + sv * TILE_BYTES + s * 2048, HALF_BYTES, 1024);
+                            mma_ts(tmem + COL_O, pcol + s * 8, bv, IDESC_PV, (npv > 0 || s > 0) ? 1u : 0u);
+                        }
+                        mma_commit(bar(B_VE + sv));
+                        mma_commit(bar(B_SFREE + pbuf));
+                        if (npv == ntiles - 1) mma_commit(bar(B_OFIN));
+                        ++npv;
+                        progressed = true;
                     }
-                    mma_commit(bar(B_VE + sv));
-                    mma_commit(bar(B_SFREE + pbuf));
-                    mma_commit(bar(B_OD));
-                    if (jp == ntiles - 1) mma_commit(bar(B_OFIN));
+                }
+                if (progressed) {
+                    t0 = clock64();
+                } else if (__nanosleep(20), *abort_flag) {  // yield issue slots to the softmax warp on this SMSP
+                    ok = false;
+                } else if (clock64() - t0 > WAIT_LIMIT) {
+                    *abort_flag = 1;
+                    ok = false;
                 }
             }
             if (!ok) {
@@ -386,7 +399,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             const float m_new = need ? mx : m_used;
             const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
             if (j > 0 && __any_sync(FULL, need)) {
-                ok = __all_sync(FULL, mbar_wait(bar(B_OD), (j - 1) & 1, abort_flag, WAIT_LIMIT));
+                // O must hold P.V_{j-1} before it is rescaled.  Its completion is
+                // tracked by the free barrier of that tile's S buffer; the S_j
+                // commit already implies P.V_{j-1-SBUF}.. so that barrier is at
+                // most one phase behind the one awaited.
+                ok = __all_sync(FULL, mbar_wait(bar(B_SFREE + (j - 1) % SBUF), ((j - 1) / SBUF) & 1, abort_flag,
+                                                WAIT_LIMIT));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -431,11 +449,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             mbar_arrive(bar(B_PF + sbuf));
         }
-        // The final O waits on its own single-use barrier.  B_OD completes once
-        // per P.V, and when the epilogue arrives the last two P.V may both be
-        // in flight, so a parity wait on B_OD could alias an older phase.
-        // (The rescale waits on B_OD above are safe: the S_j commit they follow
-        // implies every earlier MMA, so B_OD is at most one phase behind.)
+        // The final O waits on its own single-use barrier: several P.V may still
+        // be in flight here, so a parity wait on a per-tile barrier could
+        // alias an older phase.
         if (ok) ok = __all_sync(FULL, mbar_wait(bar(B_OFIN), 0, abort_flag, WAIT_LIMIT));
         if (ok) {
             tc_fence_after();

@@ -51,6 +51,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (test_wait never suspends the
+// thread, unlike try_wait), for loops that poll several barriers.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up after
 // `limit` SM clock cycles, or as soon as *abort becomes nonzero; on giving
 // up it sets *abort and returns false.
