@@ -177,15 +177,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 4);
     auto bar = [&](int i) { return sb + OFF_BAR + 8u * uint32_t(i); };
 
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int mt = p.n_mtiles - 1 - int(blockIdx.x);  // the tiles with the most keys start first
+    // CTAs launch in blockIdx.x-fastest order: x walks (head, sequence) and y
+    // the query tile from the last one down, so across the whole batch the
+    // tiles with the most keys start first
+    const int h = int(blockIdx.x) % p.num_heads, b = int(blockIdx.x) / p.num_heads;
+    const int mt = p.n_mtiles - 1 - int(blockIdx.y);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
     const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
     const bool paged = p.block_table != nullptr;
     const bool bad_shape = lk < lq || (!paged && (lk != lq || k0 != q0)) ||
                            (paged && int64_t(lk) > int64_t(p.max_blocks) * p.block_size);
-    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
+    if (blockIdx.y == 0 && h == 0 && threadIdx.x == 0) {
         if (bad_shape) pa::report(p.status, (lk < lq || !paged) ? PA_ERR_INVALID_ARG : PA_ERR_BOUNDS);
         else if (lq > p.max_q) pa::report(p.status, PA_ERR_BOUNDS);
     }
@@ -547,7 +550,7 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
         if (!pa::aligned(k_cache, 16) || !pa::aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
         if (num_blocks * block_size >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
     }
-    if (num_seqs > 65535 || num_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (int64_t(num_seqs) * num_heads > 0x7fffffff || (max_seqlen_q + BM - 1) / BM > 65535) return PA_ERR_UNSUPPORTED;
 
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -582,7 +585,7 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
         attr_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    const dim3 grid(unsigned(p.n_mtiles), unsigned(num_heads), unsigned(num_seqs));
+    const dim3 grid(unsigned(num_heads * num_seqs), unsigned(p.n_mtiles));
     prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(p);
     return pa::launch_status();
 }
