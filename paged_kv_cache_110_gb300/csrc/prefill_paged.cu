@@ -50,7 +50,7 @@ constexpr int D = pa::kHeadDim;
 constexpr int BM = 128;             // queries per CTA (TMEM lanes)
 constexpr int BN = 128;             // keys per tile
 constexpr int KSTAGES = 2;          // K tiles in flight (released as soon as S = Q K^T is done)
-constexpr int VSTAGES = 3;          // V tiles in flight (released after O += P V, so kept longer)
+constexpr int VSTAGES = 4;          // V tiles in flight (released after O += P V, so kept longer)
 constexpr int SBUF = 3;             // TMEM S buffers (P is written back over S)
 constexpr int NTHREADS = 256;
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
@@ -73,9 +73,9 @@ enum {
     NBAR = B_DRAIN + 1
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int TABLE_SMEM = 2048;                  // block-table entries staged in shared memory
+constexpr int TABLE_SMEM = 512;                   // block-table entries staged in shared memory
 constexpr int OFF_TABLE = OFF_MISC + 16;
-constexpr int SMEM_BYTES = OFF_TABLE + TABLE_SMEM * 4 + 1024;  // + slack to align the base to 1024 bytes
+constexpr int SMEM_BYTES = OFF_TABLE + TABLE_SMEM * 4;  // the base is 1024-byte aligned (checked)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 384;     // S buffers at columns 0, 128, 256
 constexpr long long WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
@@ -170,8 +170,8 @@ __device__ __forceinline__ void load_tile(const TileSource &src, int xcol, int j
 
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const uint32_t sb = smem_u32(smem);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 4);
@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     }
     if (lq <= 0 || mt * BM >= lq || bad_shape) return;
 
+    // the 128-byte swizzle pattern of TMA and the tensor cores is anchored at 1024-byte boundaries
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) pa::report(p.status, PA_ERR_UNSUPPORTED);
+        return;
+    }
     const int g = h / (p.num_heads / p.kv_heads);
     const int m0 = mt * BM;
     const int rows = min(BM, lq - m0);
