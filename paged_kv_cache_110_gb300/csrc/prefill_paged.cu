@@ -13,8 +13,9 @@
 // 128 rows, query head, sequence), heaviest query tiles first across the
 // batch.  The roles below run ahead across item boundaries, so the next
 // item's block ids, Q tile and first K/V tiles load, and its first S is
-// computed, while the current item finishes and its epilogue runs.  Q, O and
-// the staged block ids are double-buffered for that.
+// computed, while the current item finishes and its epilogue runs.  Q and
+// the staged block ids are double-buffered for that, and the epilogue hands
+// O back as soon as it has read it into registers.
 //   warp 3      stages each item's block ids (validated) in shared memory.
 //   warp 0      producer: the Q tile (cp.async) and the K tiles.  Paged keys
 //               arrive by TMA, one box per page run (box height
@@ -41,6 +42,7 @@
 // what it issued, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -56,7 +58,9 @@ constexpr int BM = 128;             // queries per work item (TMEM lanes)
 constexpr int BN = 128;             // keys per tile
 constexpr int KSTAGES = 2;          // K tiles in flight (released as soon as S = Q K^T is done)
 constexpr int VSTAGES = 3;          // V tiles in flight (released after O += P V, so kept longer)
-constexpr int SBUF = 2;             // TMEM S buffers (P is written back over S)
+constexpr int SBUF = 3;             // TMEM S buffers (P is written back over S)
+constexpr int RING = 4;             // work items fetched ahead by the scheduler warp
+static_assert(VSTAGES == SBUF, "a V stage is released by the S-buffer-free barrier of the same tile");
 constexpr int NTHREADS = 256;
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
 constexpr int TILE_BYTES = 2 * HALF_BYTES;  // 128 rows x 128 bf16
@@ -68,25 +72,25 @@ enum {
     B_QF = 0,                    // Q buffer loaded (32 arrivals)
     B_QE = B_QF + 2,             // Q buffer free (its item's last S done)
     B_KF = B_QE + 2,
-    B_KE = B_KF + KSTAGES,
-    B_VF = B_KE + KSTAGES,
-    B_VE = B_VF + VSTAGES,
-    B_SF = B_VE + VSTAGES,       // S buffer computed
+    B_VF = B_KF + KSTAGES,
+    B_SF = B_VF + VSTAGES,       // S buffer computed (also frees the K stage that S read)
     B_PF = B_SF + SBUF,          // P written over S (128 arrivals)
-    B_SE = B_PF + SBUF,          // S buffer free (the P.V reading its P done)
-    B_OF = B_SE + SBUF,          // O buffer complete (its item's last P.V done)
-    B_OE = B_OF + 2,             // O buffer free (epilogue read it, 128 arrivals)
-    B_TF = B_OE + 2,             // block-id buffer staged (32 arrivals)
+    B_SE = B_PF + SBUF,          // S buffer free: the P.V reading its P done (also frees that V stage)
+    B_OF = B_SE + SBUF,          // O complete (the item's last P.V done)
+    B_OE = B_OF + 1,             // O free (the epilogue has read it, 128 arrivals)
+    B_TF = B_OE + 1,             // block-id buffer staged (32 arrivals)
     B_TE = B_TF + 2,             // block-id buffer free (both producers done, 2 arrivals)
-    B_DRAIN = B_TE + 2,
+    B_IRF = B_TE + 2,            // item-ring slot published (1 arrival)
+    B_IRE = B_IRF + RING,        // item-ring slot read by every role (7 arrivals)
+    B_DRAIN = B_IRE + RING,
     NBAR = B_DRAIN + 1
 };
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag, item ring
 constexpr int TABLE_SMEM = 256;                   // block ids staged per item (more: read from global)
-constexpr int OFF_TABLE = OFF_MISC + 16;          // two buffers
+constexpr int OFF_TABLE = OFF_MISC + 32;          // two buffers
 constexpr int SMEM_BYTES = OFF_TABLE + 2 * TABLE_SMEM * 4;  // the base is 1024-byte aligned (checked)
-constexpr uint32_t TMEM_COLS = 512;                  // S buffers at 0 and 128, O buffers at 256 and 384
-constexpr uint32_t COL_O = 256;
+constexpr uint32_t TMEM_COLS = 512;                  // S buffers at 0, 128 and 256, O at 384
+constexpr uint32_t COL_O = 384;
 constexpr long long WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -116,7 +120,16 @@ struct TcParams {
     float scale_log2;
     uint16_t *out;
     int32_t *status;
+    unsigned int sched_slot;  // which scheduler counter pair this call uses
 };
+
+// Work-item counters, one pair [next item, CTAs finished] per call in flight.
+// Each launch takes the next pair round-robin; they start at zero (static
+// storage) and the last CTA of a launch sets its pair back to zero, so a launch
+// always finds its pair at zero unless SCHED_SLOTS later launches were issued
+// while it still runs on another stream.
+constexpr unsigned SCHED_SLOTS = 4096;
+__device__ unsigned int g_prefill_sched[SCHED_SLOTS][2];
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk)  // byte offset in a 128-row, 128-byte-row block
 {
@@ -239,6 +252,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     auto bar = [&](int i) { return sb + OFF_BAR + 8u * uint32_t(i); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the 128-byte swizzle pattern of TMA and the tensor cores is anchored at 1024-byte boundaries
+    // (every CTA of a launch sees the same alignment, so none has touched the counters)
     if ((sb & 1023u) != 0) {
         if (threadIdx.x == 0) pa::report(p.status, PA_ERR_UNSUPPORTED);
         return;
@@ -252,18 +266,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_QF + i), 32);
             mbar_init(bar(B_QE + i), 1);
-            mbar_init(bar(B_OF + i), 1);
-            mbar_init(bar(B_OE + i), 128);
             mbar_init(bar(B_TF + i), 32);
             mbar_init(bar(B_TE + i), 2);
         }
-        for (int s = 0; s < KSTAGES; ++s) {
-            mbar_init(bar(B_KF + s), loader_count);
-            mbar_init(bar(B_KE + s), 1);
-        }
-        for (int s = 0; s < VSTAGES; ++s) {
-            mbar_init(bar(B_VF + s), loader_count);
-            mbar_init(bar(B_VE + s), 1);
+        mbar_init(bar(B_OF), 1);
+        mbar_init(bar(B_OE), 128);
+        for (int s = 0; s < KSTAGES; ++s) mbar_init(bar(B_KF + s), loader_count);
+        for (int s = 0; s < VSTAGES; ++s) mbar_init(bar(B_VF + s), loader_count);
+        for (int s = 0; s < RING; ++s) {
+            mbar_init(bar(B_IRF + s), 1);
+            mbar_init(bar(B_IRE + s), 7);
         }
         for (int s = 0; s < SBUF; ++s) {
             mbar_init(bar(B_SF + s), 1);
@@ -283,31 +295,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 16);
     if (warp == 3) {
-        // ------------------------------------------------------------ block-id stager
-        int n = 0;  // valid items seen
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-            const Item it = decode_item(p, w);
-            if (it.bad && lane == 0) pa::report(p.status, it.bad_code);
-            if (!it.valid) continue;
-            const int tb = n & 1;
-            if (n >= 2 && !mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)) break;
-            if (paged) {
-                const int nblk = (it.kend + p.block_size - 1) / p.block_size;
-                const int32_t *gtable = p.block_table + int64_t(it.b) * p.max_blocks;
-                int32_t *st = reinterpret_cast<int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM;
-                bool bad = false;
-                for (int i = lane; i < nblk; i += 32) {
-                    int32_t phys = gtable[i];
-                    if (phys < 0 || int64_t(phys) >= p.num_blocks) {
-                        bad = true;
-                        phys = -1;
-                    }
-                    if (nblk <= TABLE_SMEM) st[i] = phys;
+        // ------------------------------------------------------------ scheduler
+        // Fetch work items from the call's counter (heaviest first), publish each
+        // in the item ring and stage its block ids (validated) for the producers.
+        int n = 0;  // items published
+        while (true) {
+            int w = -1;
+            while (true) {
+                int cand = 0;
+                if (lane == 0) cand = int(atomicAdd(&g_prefill_sched[p.sched_slot][0], 1u));
+                cand = __shfl_sync(FULL, cand, 0);
+                if (cand >= n_items) break;
+                const Item it = decode_item(p, cand);
+                if (it.bad && lane == 0) pa::report(p.status, it.bad_code);
+                if (it.valid) {
+                    w = cand;
+                    break;
                 }
-                if (bad) pa::report(p.status, PA_ERR_BOUNDS);
             }
-            mbar_arrive(bar(B_TF + tb));
+            const int slot = n % RING, tb = n & 1;
+            if (n >= RING && !mbar_wait(bar(B_IRE + slot), par(n - RING, RING), abort_flag, WAIT_LIMIT)) break;
+            if (w >= 0) {
+                if (n >= 2 && !mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)) break;
+                if (paged) {
+                    const Item it = decode_item(p, w);
+                    const int nblk = (it.kend + p.block_size - 1) / p.block_size;
+                    const int32_t *gtable = p.block_table + int64_t(it.b) * p.max_blocks;
+                    int32_t *st = reinterpret_cast<int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM;
+                    bool bad = false;
+                    for (int i = lane; i < nblk; i += 32) {
+                        int32_t phys = gtable[i];
+                        if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+                            bad = true;
+                            phys = -1;
+                        }
+                        if (nblk <= TABLE_SMEM) st[i] = phys;
+                    }
+                    if (bad) pa::report(p.status, PA_ERR_BOUNDS);
+                }
+                mbar_arrive(bar(B_TF + tb));
+            }
+            if (lane == 0) {
+                ring[slot] = w;
+                mbar_arrive(bar(B_IRF + slot));
+            }
+            if (w < 0) break;
             ++n;
         }
     } else if (warp == 0 || warp == 2) {
@@ -322,12 +356,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         if (paged && lane == 0) tma_prefetch_desc(src.map);
         const int nst = is_k ? KSTAGES : VSTAGES;
         const uint32_t base = sb + (is_k ? OFF_K : OFF_V);
-        const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_KE : B_VE;
-        int n = 0, t = 0;  // valid items, tiles issued
+        // a K stage is free once the S that read it is done, a V stage once the
+        // P.V that read it is done (SBUF == VSTAGES keeps their indices equal)
+        const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_SF : B_SE;
+        int n = 0, t = 0;  // items, tiles issued
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        for (;; ++n) {
+            const int slot = n % RING;
+            if (!(ok = mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) break;
+            const int w = ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+            if (w < 0) break;
             const Item it = decode_item(p, w);
-            if (!it.valid) continue;
             const int tb = n & 1;
             if (!(ok = mbar_wait(bar(B_TF + tb), par(n, 2), abort_flag, WAIT_LIMIT))) break;
             const int nblk = paged ? (it.kend + p.block_size - 1) / p.block_size : 0;
@@ -338,7 +379,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             src.rows = paged ? nullptr : (is_k ? p.k : p.v) + int64_t(it.k0) * p.kv_stride + g * D;
             for (int j = 0; j < it.ntiles; ++j, ++t) {
                 const int st = t % nst;
-                if (t >= nst && !(ok = mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, WAIT_LIMIT))) break;
+                if (t >= nst &&
+                    !(ok = mbar_wait(bar(empty0 + (t - nst) % SBUF), par(t - nst, SBUF), abort_flag, WAIT_LIMIT)))
+                    break;
                 load_tile(src, g * D, j * BN, it.kend, base + st * TILE_BYTES, bar(full0 + st), lane, p.num_blocks);
                 if (is_k && j == 0) {
                     // this item's Q tile, rows past the sequence zero-filled
@@ -358,7 +401,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             }
             if (!ok) break;
             if (lane == 0) mbar_arrive(bar(B_TE + tb));  // this producer no longer reads the block ids
-            ++n;
         }
         if (*abort_flag && paged && lane == 0) {
             // let copies already in flight land before the CTA's shared memory goes away
@@ -371,26 +413,58 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
-            // S cursor: item sw (count sn), tile sj, global tile ts; P.V cursor likewise
-            int sw = blockIdx.x, sn = 0, sj = 0, ts = 0;
-            int pw = blockIdx.x, pn = 0, pj = 0, tp = 0;
+            // S cursor: item count sn, tile sj, global tile ts; P.V cursor likewise.
+            // Both read the item ring; the P.V cursor (the later one) frees the slot.
+            int sn = 0, sj = 0, ts = 0;
+            int pn = 0, pj = 0, tp = 0;
             Item si, pi;
-            si.valid = pi.valid = false;
-            auto next_valid = [&](int &w, Item &it) {
-                while (w < n_items) {
-                    it = decode_item(p, w);
-                    if (it.valid) return true;
-                    w += gridDim.x;
-                }
-                return false;
-            };
-            bool s_live = next_valid(sw, si), p_live = next_valid(pw, pi);
             bool ok = true;
+            auto read_item = [&](int n, Item &it, bool release) {
+                const int slot = n % RING;
+                if (!mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT)) {
+                    ok = false;
+                    return false;
+                }
+                const int w = ring[slot];
+                if (release) mbar_arrive(bar(B_IRE + slot));
+                if (w < 0) return false;
+                it = decode_item(p, w);
+                return true;
+            };
+            bool s_live = read_item(0, si, false), p_live = read_item(0, pi, true);
             long long t0 = clock64();
             while (ok && p_live) {
                 bool progressed = false;
-                // S: K tile in, Q of the item in, S buffer free, at most SBUF ahead of P.V
-                if (s_live && ts - tp < SBUF) {
+                // Issue blocks while the tensor pipe is busy (its queue is short), so
+                // the issue order is the execution order.  The order kept is
+                // P.V_j, S_{j+2}, P.V_{j+1}, ...: at most one S ahead of the next P.V,
+                // so S_{j+1} runs during the softmax of tile j and P.V_j is never
+                // queued behind two S.
+                // P.V: P and V in, and for the item's first tile O free.
+                if (tp < ts) {
+                    const int sv = tp % VSTAGES, pbuf = tp % SBUF;
+                    if (mbar_poll(bar(B_PF + pbuf), par(tp, SBUF)) && mbar_poll(bar(B_VF + sv), par(tp, VSTAGES)) &&
+                        (pj > 0 || pn < 1 || mbar_poll(bar(B_OE), par(pn - 1, 1)))) {
+                        tc_fence_after();
+                        const uint32_t vs = sb + OFF_V + sv * TILE_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_ts(tmem + COL_O, tmem + 128u * pbuf + kk * 8,
+                                   smem_desc(vs + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (pj > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar(B_SE + pbuf));
+                        ++tp;
+                        if (++pj == pi.ntiles) {
+                            mma_commit(bar(B_OF));  // the item's O is complete
+                            pj = 0;
+                            ++pn;
+                            p_live = read_item(pn, pi, true);
+                        }
+                        progressed = true;
+                    }
+                }
+                // S: K tile in, Q of the item in, S buffer free (the P.V of the tile
+                // that last used it has completed), at most one ahead of the next P.V
+                if (s_live && ts - tp < 2) {
                     const int st = ts % KSTAGES, sbuf = ts % SBUF, qb = sn & 1;
                     if (mbar_poll(bar(B_KF + st), par(ts, KSTAGES)) &&
                         (ts < SBUF || mbar_poll(bar(B_SE + sbuf), par(ts - SBUF, SBUF))) &&
@@ -405,38 +479,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                                    smem_desc(ks + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
                         }
                         mma_commit(bar(B_SF + sbuf));
-                        mma_commit(bar(B_KE + st));
                         ++ts;
                         if (++sj == si.ntiles) {
                             mma_commit(bar(B_QE + qb));  // the item's Q tile is no longer read
                             sj = 0;
                             ++sn;
-                            sw += gridDim.x;
-                            s_live = next_valid(sw, si);
-                        }
-                        progressed = true;
-                    }
-                }
-                // P.V: P and V in, and for the item's first tile its O buffer free
-                if (tp < ts) {
-                    const int sv = tp % VSTAGES, pbuf = tp % SBUF, ob = pn & 1;
-                    if (mbar_poll(bar(B_PF + pbuf), par(tp, SBUF)) && mbar_poll(bar(B_VF + sv), par(tp, VSTAGES)) &&
-                        (pj > 0 || pn < 2 || mbar_poll(bar(B_OE + ob), par(pn - 2, 2)))) {
-                        tc_fence_after();
-                        const uint32_t vs = sb + OFF_V + sv * TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + COL_O + 128u * ob, tmem + 128u * pbuf + kk * 8,
-                                   smem_desc(vs + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (pj > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(bar(B_VE + sv));
-                        mma_commit(bar(B_SE + pbuf));
-                        ++tp;
-                        if (++pj == pi.ntiles) {
-                            mma_commit(bar(B_OF + ob));  // the item's O is complete
-                            pj = 0;
-                            ++pn;
-                            pw += gridDim.x;
-                            p_live = next_valid(pw, pi);
+                            s_live = read_item(sn, si, false);
                         }
                         progressed = true;
                     }
@@ -464,13 +512,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         const int r = quarter * 32 + lane;
         const uint32_t lane_base = uint32_t(quarter * 32) << 16;
         const float sl2 = p.scale_log2;
-        int n = 0, ts = 0;  // valid items, global tile index
+        int ts = 0;  // global tile index
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        for (int n = 0;; ++n) {
+            const int slot = n % RING;
+            ok = __all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT));
+            if (!ok) break;
+            const int w = ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+            if (w < 0) break;
             const Item it = decode_item(p, w);
-            if (!it.valid) continue;
-            const int ob = n & 1;
-            const uint32_t ocol = tmem + lane_base + COL_O + 128u * ob;
+            const uint32_t ocol = tmem + lane_base + COL_O;
             const int pos = it.offset + it.m0 + r;
             const int last_visible = min(pos, it.kend - 1);
             float m_used = -INFINITY;  // running max in scaled base-2 units
@@ -562,38 +615,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 mbar_arrive(bar(B_PF + sbuf));
             }
             if (!ok) break;
-            // epilogue: the item's O is complete once its own barrier fires
-            ok = __all_sync(FULL, mbar_wait(bar(B_OF + ob), par(n, 2), abort_flag, WAIT_LIMIT));
+            // epilogue: O is complete once its own barrier fires (a single-use
+            // phase per item); read it all, hand it back, then normalise and store
+            ok = __all_sync(FULL, mbar_wait(bar(B_OF), par(n, 1), abort_flag, WAIT_LIMIT));
             if (!ok) break;
             tc_fence_after();
+            uint32_t o[128];
+            tmem_ld128_sync(ocol, o);
+            tc_fence_before();
+            mbar_arrive(bar(B_OE));  // the next item's P.V may overwrite O now
             const float inv = 1.f / l;
-            uint16_t *dst = p.out + (int64_t(it.q0 + it.m0 + r) * p.num_heads + it.h) * D;
+            if (r < it.rows) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(p.out + (int64_t(it.q0 + it.m0 + r) * p.num_heads + it.h) * D);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t o[32];
-                tmem_ld32_sync(ocol + cc * 32, o);
-                if (r < it.rows) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 u;
-                        u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        d4[v] = u;
-                    }
+                for (int v = 0; v < 16; ++v) {
+                    uint4 u;
+                    u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    d4[v] = u;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(B_OE + ob));  // the O buffer may be overwritten now
-            ++n;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) pa::report(p.status, PA_ERR_TIMEOUT);
+    if (threadIdx.x == 0) {
+        if (*abort_flag) pa::report(p.status, PA_ERR_TIMEOUT);
+        // the last CTA to finish leaves the call's counters at zero for the next call
+        unsigned int *ctr = g_prefill_sched[p.sched_slot];
+        __threadfence();
+        if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+            atomicExch(ctr, 0u);
+            atomicExch(ctr + 1, 0u);
+        }
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -685,6 +743,8 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
     p.scale_log2 = scale * LOG2E;
     p.out = static_cast<uint16_t *>(out);
     p.status = dev_status;
+    static std::atomic<unsigned> next_slot{0};
+    p.sched_slot = next_slot.fetch_add(1u, std::memory_order_relaxed) % SCHED_SLOTS;
     if (block_table != nullptr) {
         const int64_t rows = num_blocks * block_size;
         if (!make_pool_map(&p.kmap, k_cache, rows, num_kv_heads, p.box_rows) ||
