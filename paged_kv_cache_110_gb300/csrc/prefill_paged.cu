@@ -9,35 +9,35 @@
 // reads KV head h / (Hq / Hkv) (§19.6).  Softmax is accumulated blockwise with
 // a running max, a running sum and an unnormalised numerator (§13.3).
 //
-// A persistent kernel: one CTA per SM walks the work items (query tile of
-// 128 rows, query head, sequence), heaviest query tiles first across the
-// batch.  The roles below run ahead across item boundaries, so the next
-// item's block ids, Q tile and first K/V tiles load, and its first S is
-// computed, while the current item finishes and its epilogue runs.  Q and
-// the staged block ids are double-buffered for that, and the epilogue hands
-// O back as soon as it has read it into registers.
-//   warp 3      stages each item's block ids (validated) in shared memory.
-//   warp 0      producer: the Q tile (cp.async) and the K tiles.  Paged keys
-//               arrive by TMA, one box per page run (box height
-//               gcd(block_size, 128) rows, so a box never crosses a page);
-//               without a table rows are copied with cp.async.  All tiles land
-//               in shared memory in the 128-byte-swizzled layout the tensor
-//               cores read.  A K stage is reused once its S is done.
-//   warp 2      producer: the V tiles; a V stage is reused once its P.V is done.
-//   warp 1      MMA issuer (one thread, a polling state machine): S = Q K^T
-//               into one of two TMEM S buffers (M = N = 128, K = 128) and
-//               O += P V into the item's TMEM O buffer with P read back from
-//               TMEM; S runs up to two tiles ahead of P.V.  A TMEM region is
-//               rewritten only after the MMA reading it has completed.
-//   warps 4-7   softmax, one thread per query row: read the S row from TMEM,
-//               mask (causal, bottom-right, and keys past the tile's last
-//               visible key), row max, then base-2 exponentials with
+// A persistent kernel: one CTA per SM takes work items from a device counter,
+// heaviest first.  An item is a PAIR of 128-row query tiles that read the same
+// keys: the same rows of two query heads of one KV group (GQA), or, when every
+// KV head has a single query head, two consecutive row tiles of one head.
+// Each K and V tile is loaded once for both, and while one tile's softmax runs
+// the tensor cores work on the other's, so the two dependency chains
+// (S -> softmax -> P.V) hide each other.
+//   warp 3      scheduler: fetches items, publishes them in a ring of 4,
+//               stages each item's block ids (validated) and loads its two Q
+//               tiles (cp.async, rows past the sequence zero-filled) into a
+//               ring of three Q buffers.
+//   warp 0      K producer, warp 2 V producer: paged tiles arrive by TMA, one
+//               box per page run (box height gcd(block_size, 128) rows, so a
+//               box never crosses a page); without a table rows are copied with
+//               cp.async.  Tiles land in shared memory in the 128-byte-swizzled
+//               layout the tensor cores read; two stages each.
+//   warp 1      MMA issuer (one thread): per K/V tile j, O_0 += P_0 V_j then
+//               S_0 = Q_0 K_{j+1}^T, then the same for query tile 1.  S and O of
+//               each query tile live in TMEM (S at columns 0 / 128, O at
+//               256 / 384); P is written back over S, and the next S is issued
+//               after the P.V that reads P (tcgen05 operations run in order).
+//   warps 4-7, 8-11   softmax of query tile 0 and 1, one thread per row: read
+//               the S row from TMEM, mask (causal, bottom-right, keys past the
+//               last visible key), row max, base-2 exponentials with
 //               scale * log2(e) folded into paired FMAs, row sums, P as bf16
-//               written back over S.  The running max is raised only when a
-//               row max grows by more than 8 (a factor 256), and only then is
-//               the O row rescaled in TMEM; the final O / l uses the same max,
-//               so the result is exact.  Epilogue: O / l to bf16, one row per
-//               thread, then the O buffer is handed back.
+//               over S.  The running max is raised only when a row max grows
+//               by more than 8 (a factor 256), and only then is the O row
+//               rescaled in TMEM; O / l uses the same max, so the result is
+//               exact.  Epilogue: O / l to bf16, one row per thread.
 // Every wait is bounded: on a timeout the CTA records PA_ERR_TIMEOUT, drains
 // what it issued, frees its TMEM and exits.
 #include <cudaTypedefs.h>
@@ -54,43 +54,47 @@ namespace {
 using namespace pa::sm100;
 
 constexpr int D = pa::kHeadDim;
-constexpr int BM = 128;             // queries per work item (TMEM lanes)
+constexpr int BM = 128;             // query rows per query tile (TMEM lanes)
+constexpr int QT = 2;               // query tiles per work item, sharing every K/V tile
 constexpr int BN = 128;             // keys per tile
-constexpr int KSTAGES = 2;          // K tiles in flight (released as soon as S = Q K^T is done)
-constexpr int VSTAGES = 3;          // V tiles in flight (released after O += P V, so kept longer)
-constexpr int SBUF = 3;             // TMEM S buffers (P is written back over S)
+constexpr int KSTAGES = 2;          // K tiles in flight
+constexpr int VSTAGES = 2;          // V tiles in flight
+constexpr int QSLOTS = 3;           // Q tile buffers: one item's pair and the next item's first tile
 constexpr int RING = 4;             // work items fetched ahead by the scheduler warp
-static_assert(VSTAGES == SBUF, "a V stage is released by the S-buffer-free barrier of the same tile");
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 384;
+constexpr uint32_t REGS_CONTROL = 96;   // per thread, warps 0-3 (one warpgroup)
+constexpr uint32_t REGS_SOFTMAX = 200;  // per thread, warps 4-11
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
 constexpr int TILE_BYTES = 2 * HALF_BYTES;  // 128 rows x 128 bf16
-constexpr int OFF_Q = 0;                    // two Q buffers
-constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + QSLOTS * TILE_BYTES;
 constexpr int OFF_V = OFF_K + KSTAGES * TILE_BYTES;
 constexpr int OFF_BAR = OFF_V + VSTAGES * TILE_BYTES;
 enum {
     B_QF = 0,                    // Q buffer loaded (32 arrivals)
-    B_QE = B_QF + 2,             // Q buffer free (its item's last S done)
-    B_KF = B_QE + 2,
-    B_VF = B_KF + KSTAGES,
-    B_SF = B_VF + VSTAGES,       // S buffer computed (also frees the K stage that S read)
-    B_PF = B_SF + SBUF,          // P written over S (128 arrivals)
-    B_SE = B_PF + SBUF,          // S buffer free: the P.V reading its P done (also frees that V stage)
-    B_OF = B_SE + SBUF,          // O complete (the item's last P.V done)
-    B_OE = B_OF + 1,             // O free (the epilogue has read it, 128 arrivals)
-    B_TF = B_OE + 1,             // block-id buffer staged (32 arrivals)
+    B_QE = B_QF + QSLOTS,        // Q buffer free (its tile's last S done)
+    B_KF = B_QE + QSLOTS,        // K stage loaded
+    B_KE = B_KF + KSTAGES,       // K stage free (every S reading it done)
+    B_VF = B_KE + KSTAGES,       // V stage loaded
+    B_VE = B_VF + VSTAGES,       // V stage free (every P.V reading it done)
+    B_SF = B_VE + VSTAGES,       // S of query tile a computed, per a
+    B_PF = B_SF + QT,            // P of query tile a written over its S (128 arrivals), per a
+    B_OF = B_PF + QT,            // O of query tile a complete for the item, per a
+    B_TF = B_OF + QT,            // block-id buffer staged (32 arrivals)
     B_TE = B_TF + 2,             // block-id buffer free (both producers done, 2 arrivals)
     B_IRF = B_TE + 2,            // item-ring slot published (1 arrival)
-    B_IRE = B_IRF + RING,        // item-ring slot read by every role (7 arrivals)
+    B_IRE = B_IRF + RING,        // item-ring slot read by every role (11 arrivals)
     B_DRAIN = B_IRE + RING,
     NBAR = B_DRAIN + 1
 };
+constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA thread, softmax warps
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag, item ring
 constexpr int TABLE_SMEM = 256;                   // block ids staged per item (more: read from global)
 constexpr int OFF_TABLE = OFF_MISC + 32;          // two buffers
 constexpr int SMEM_BYTES = OFF_TABLE + 2 * TABLE_SMEM * 4;  // the base is 1024-byte aligned (checked)
-constexpr uint32_t TMEM_COLS = 512;                  // S buffers at 0, 128 and 256, O at 384
-constexpr uint32_t COL_O = 384;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t TMEM_COLS = 512;                  // S of tiles 0 / 1 at 0 / 128, O at 256 / 384
+constexpr uint32_t COL_O = 256;
 constexpr long long WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -114,6 +118,9 @@ struct TcParams {
     const int32_t *cu_k;
     int max_q;
     int n_mtiles;
+    int n_steps;      // item rows: query tiles (head pairs) or query-tile pairs (single heads)
+    int units;        // items per sequence and step: head pairs, or heads
+    int pair_heads;   // 1: an item's two tiles are two query heads; 0: two row tiles of one head
     int num_heads;
     int num_seqs;
     int kv_heads;
@@ -139,23 +146,26 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk)  // byte offset i
 // Parity of completion number n of a barrier used by every nbuf-th round.
 __device__ __forceinline__ uint32_t par(int n, int nbuf) { return uint32_t(n / nbuf) & 1u; }
 
-// One work item: a 128-row query tile of one (sequence, query head).
+// One work item: two 128-row query tiles of one sequence that read the same
+// KV head.  A tile with rows == 0 is empty (nt == 0).
 struct Item {
-    int b, h, m0, rows, q0, k0, offset, kend, ntiles;
+    int b, g, q0, k0, offset;
+    int h[QT], m0[QT], rows[QT], kend[QT], nt[QT];
+    int nmax, kend_max;  // K/V tiles and keys the item reads
     bool valid, bad;
     int bad_code;
 };
 
-// Items are numbered so that consecutive numbers walk (head, sequence) and
-// then the query tile from the last one down: the heaviest tiles come first.
+// Items are numbered so that consecutive numbers walk (unit, sequence) and
+// then the step from the last one down: the heaviest tiles come first.
 __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
 {
     Item it;
-    const int hb = p.num_heads * p.num_seqs;
-    const int y = w / hb, x = w % hb;
-    it.h = x % p.num_heads;
-    it.b = x / p.num_heads;
-    const int mt = p.n_mtiles - 1 - y;
+    const int xb = p.units * p.num_seqs;
+    const int y = w / xb, x = w % xb;
+    const int u = x % p.units;
+    it.b = x / p.units;
+    const int step = p.n_steps - 1 - y;
     it.q0 = p.cu_q[it.b];
     const int lq = p.cu_q[it.b + 1] - it.q0;
     it.k0 = p.cu_k[it.b];
@@ -164,16 +174,27 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
     it.bad = lk < lq || (!paged && (lk != lq || it.k0 != it.q0)) ||
              (paged && int64_t(lk) > int64_t(p.max_blocks) * p.block_size);
     it.bad_code = (lk < lq || !paged) ? PA_ERR_INVALID_ARG : PA_ERR_BOUNDS;
-    it.valid = lq > 0 && mt * BM < lq && !it.bad;
-    it.m0 = mt * BM;
-    it.rows = min(BM, lq - it.m0);
     it.offset = lk - lq;
-    it.kend = it.offset + it.m0 + it.rows;
-    it.ntiles = (it.kend + BN - 1) / BN;
-    if (lq > p.max_q && !it.bad) {  // reported; rows beyond the stated bound are not computed
+    // rows beyond the stated maximum are not computed (the call reports it)
+    const int lq_c = min(lq, p.max_q);
+    it.nmax = 0;
+    it.kend_max = 0;
+#pragma unroll
+    for (int a = 0; a < QT; ++a) {
+        const int mt = p.pair_heads ? step : 2 * step + a;
+        it.h[a] = p.pair_heads ? 2 * u + a : u;
+        it.m0[a] = mt * BM;
+        it.rows[a] = max(0, min(BM, lq_c - it.m0[a]));
+        it.kend[a] = it.rows[a] > 0 ? it.offset + it.m0[a] + it.rows[a] : 0;
+        it.nt[a] = (it.kend[a] + BN - 1) / BN;
+        it.nmax = max(it.nmax, it.nt[a]);
+        it.kend_max = max(it.kend_max, it.kend[a]);
+    }
+    it.g = it.h[0] / (p.num_heads / p.kv_heads);
+    it.valid = it.rows[0] > 0 && !it.bad;
+    if (lq > p.max_q && !it.bad) {
         it.bad = true;
         it.bad_code = PA_ERR_BOUNDS;
-        it.valid = lq > 0 && mt * BM < lq;
     }
     return it;
 }
@@ -249,6 +270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const uint32_t sb = smem_u32(smem);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 4);
+    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 16);
     auto bar = [&](int i) { return sb + OFF_BAR + 8u * uint32_t(i); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the 128-byte swizzle pattern of TMA and the tensor cores is anchored at 1024-byte boundaries
@@ -258,29 +280,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         return;
     }
     const bool paged = p.block_table != nullptr;
-    const int n_items = p.n_mtiles * p.num_heads * p.num_seqs;
-    const int group = p.num_heads / p.kv_heads;
+    const int n_items = p.n_steps * p.units * p.num_seqs;
 
     if (threadIdx.x == 0) {
         const uint32_t loader_count = paged ? 1 : 32;
+        for (int s = 0; s < QSLOTS; ++s) {
+            mbar_init(bar(B_QF + s), 32);
+            mbar_init(bar(B_QE + s), 1);
+        }
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(bar(B_KF + s), loader_count);
+            mbar_init(bar(B_KE + s), 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(bar(B_VF + s), loader_count);
+            mbar_init(bar(B_VE + s), 1);
+        }
+        for (int a = 0; a < QT; ++a) {
+            mbar_init(bar(B_SF + a), 1);
+            mbar_init(bar(B_PF + a), 128);
+            mbar_init(bar(B_OF + a), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_QF + i), 32);
-            mbar_init(bar(B_QE + i), 1);
             mbar_init(bar(B_TF + i), 32);
             mbar_init(bar(B_TE + i), 2);
         }
-        mbar_init(bar(B_OF), 1);
-        mbar_init(bar(B_OE), 128);
-        for (int s = 0; s < KSTAGES; ++s) mbar_init(bar(B_KF + s), loader_count);
-        for (int s = 0; s < VSTAGES; ++s) mbar_init(bar(B_VF + s), loader_count);
         for (int s = 0; s < RING; ++s) {
             mbar_init(bar(B_IRF + s), 1);
-            mbar_init(bar(B_IRE + s), 7);
-        }
-        for (int s = 0; s < SBUF; ++s) {
-            mbar_init(bar(B_SF + s), 1);
-            mbar_init(bar(B_PF + s), 128);
-            mbar_init(bar(B_SE + s), 1);
+            mbar_init(bar(B_IRE + s), IR_READERS);
         }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -294,12 +321,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the softmax warpgroups hold a 64-column slice of S, its P and O rows in
+    // registers; the scheduler, producer and MMA warps need few
+    static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= 168 * NTHREADS, "register split");
+    if (warp < 4)
+        regs_decrease<REGS_CONTROL>();
+    else
+        regs_increase<REGS_SOFTMAX>();
 
-    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 16);
+    // Read item n from the ring (every lane of the calling warp waits; lane 0
+    // releases the slot).  Returns the item number, -1 at the end, -2 on abort.
+    auto read_ring = [&](int n) -> int {
+        const int slot = n % RING;
+        if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) return -2;
+        const int w = ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+        return w;
+    };
+
     if (warp == 3) {
         // ------------------------------------------------------------ scheduler
         // Fetch work items from the call's counter (heaviest first), publish each
-        // in the item ring and stage its block ids (validated) for the producers.
+        // in the item ring, stage its block ids (validated) for the producers and
+        // load its two Q tiles.
         int n = 0;  // items published
         while (true) {
             int w = -1;
@@ -316,12 +361,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 }
             }
             const int slot = n % RING, tb = n & 1;
-            if (n >= RING && !mbar_wait(bar(B_IRE + slot), par(n - RING, RING), abort_flag, WAIT_LIMIT)) break;
+            if (n >= RING &&
+                !__all_sync(FULL, mbar_wait(bar(B_IRE + slot), par(n - RING, RING), abort_flag, WAIT_LIMIT)))
+                break;
+            Item it;
             if (w >= 0) {
-                if (n >= 2 && !mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)) break;
+                it = decode_item(p, w);
+                if (n >= 2 && !__all_sync(FULL, mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)))
+                    break;
                 if (paged) {
-                    const Item it = decode_item(p, w);
-                    const int nblk = (it.kend + p.block_size - 1) / p.block_size;
+                    const int nblk = (it.kend_max + p.block_size - 1) / p.block_size;
                     const int32_t *gtable = p.block_table + int64_t(it.b) * p.max_blocks;
                     int32_t *st = reinterpret_cast<int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM;
                     bool bad = false;
@@ -342,10 +391,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 mbar_arrive(bar(B_IRF + slot));
             }
             if (w < 0) break;
+            // the item's Q tiles (rows past the sequence zero-filled) into Q buffers
+            // 2n and 2n+1 of the ring of three
+            bool ok = true;
+            for (int a = 0; a < QT && ok; ++a) {
+                const int qn = 2 * n + a, qs = qn % QSLOTS;
+                if (qn >= QSLOTS &&
+                    !(ok = __all_sync(FULL, mbar_wait(bar(B_QE + qs), par(qn - QSLOTS, QSLOTS), abort_flag,
+                                                      WAIT_LIMIT))))
+                    break;
+                if (it.rows[a] > 0) {
+                    const uint32_t dst = sb + OFF_Q + qs * TILE_BYTES;
+                    const uint16_t *src = p.q + int64_t(it.q0 + it.m0[a]) * p.q_stride + it.h[a] * D;
+                    for (int idx = lane; idx < BM * 16; idx += 32) {
+                        const int r = idx >> 4, c = idx & 15;
+                        const bool valid = r < it.rows[a];
+                        cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7),
+                                   valid ? src + int64_t(r) * p.q_stride + c * 8 : p.q, valid);
+                    }
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(bar(B_QF + qs));
+            }
+            if (!ok) break;
             ++n;
         }
     } else if (warp == 0 || warp == 2) {
-        // ------------------------------------------------------------ producers (K + Q, V)
+        // ------------------------------------------------------------ producers (K, V)
         const bool is_k = warp == 0;
         TileSource src;
         src.map = paged ? (is_k ? &p.kmap : &p.vmap) : nullptr;
@@ -354,50 +427,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         src.stride = p.kv_stride;
         src.dummy = p.q;
         if (paged && lane == 0) tma_prefetch_desc(src.map);
-        const int nst = is_k ? KSTAGES : VSTAGES;
+        constexpr int nst = KSTAGES;
+        static_assert(KSTAGES == VSTAGES, "one stage count for both producers");
         const uint32_t base = sb + (is_k ? OFF_K : OFF_V);
-        // a K stage is free once the S that read it is done, a V stage once the
-        // P.V that read it is done (SBUF == VSTAGES keeps their indices equal)
-        const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_SF : B_SE;
-        int n = 0, t = 0;  // items, tiles issued
+        const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_KE : B_VE;
+        int t = 0;  // tiles issued
         bool ok = true;
-        for (;; ++n) {
-            const int slot = n % RING;
-            if (!(ok = mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) break;
-            const int w = ring[slot];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+        for (int n = 0;; ++n) {
+            const int w = read_ring(n);
+            if (w == -2) ok = false;
             if (w < 0) break;
             const Item it = decode_item(p, w);
             const int tb = n & 1;
             if (!(ok = mbar_wait(bar(B_TF + tb), par(n, 2), abort_flag, WAIT_LIMIT))) break;
-            const int nblk = paged ? (it.kend + p.block_size - 1) / p.block_size : 0;
+            const int nblk = paged ? (it.kend_max + p.block_size - 1) / p.block_size : 0;
             src.table = (paged && nblk <= TABLE_SMEM)
                             ? reinterpret_cast<const int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM
                             : (paged ? p.block_table + int64_t(it.b) * p.max_blocks : nullptr);
-            const int g = it.h / group;
-            src.rows = paged ? nullptr : (is_k ? p.k : p.v) + int64_t(it.k0) * p.kv_stride + g * D;
-            for (int j = 0; j < it.ntiles; ++j, ++t) {
+            src.rows = paged ? nullptr : (is_k ? p.k : p.v) + int64_t(it.k0) * p.kv_stride + it.g * D;
+            for (int j = 0; j < it.nmax; ++j, ++t) {
                 const int st = t % nst;
-                if (t >= nst &&
-                    !(ok = mbar_wait(bar(empty0 + (t - nst) % SBUF), par(t - nst, SBUF), abort_flag, WAIT_LIMIT)))
+                if (t >= nst && !(ok = mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, WAIT_LIMIT)))
                     break;
-                load_tile(src, g * D, j * BN, it.kend, base + st * TILE_BYTES, bar(full0 + st), lane, p.num_blocks);
-                if (is_k && j == 0) {
-                    // this item's Q tile, rows past the sequence zero-filled
-                    const int qb = n & 1;
-                    if (n >= 2 && !(ok = mbar_wait(bar(B_QE + qb), par(n - 2, 2), abort_flag, WAIT_LIMIT))) break;
-                    for (int idx = lane; idx < BM * 16; idx += 32) {
-                        const int r = idx >> 4, c = idx & 15;
-                        const bool valid = r < it.rows;
-                        const uint16_t *qp =
-                            valid ? p.q + int64_t(it.q0 + it.m0 + r) * p.q_stride + it.h * D + c * 8 : p.q;
-                        cp_async16(sb + OFF_Q + qb * TILE_BYTES + (c >> 3) * HALF_BYTES + swz128(r, c & 7), qp, valid);
-                    }
-                    cp_async_wait_all();
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(B_QF + qb));
-                }
+                load_tile(src, it.g * D, j * BN, it.kend_max, base + st * TILE_BYTES, bar(full0 + st), lane,
+                          p.num_blocks);
             }
             if (!ok) break;
             if (lane == 0) mbar_arrive(bar(B_TE + tb));  // this producer no longer reads the block ids
@@ -410,132 +463,126 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
-            constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
-            // S cursor: item count sn, tile sj, global tile ts; P.V cursor likewise.
-            // Both read the item ring; the P.V cursor (the later one) frees the slot.
-            int sn = 0, sj = 0, ts = 0;
-            int pn = 0, pj = 0, tp = 0;
-            Item si, pi;
-            bool ok = true;
-            auto read_item = [&](int n, Item &it, bool release) {
-                const int slot = n % RING;
-                if (!mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT)) {
-                    ok = false;
-                    return false;
-                }
-                const int w = ring[slot];
-                if (release) mbar_arrive(bar(B_IRE + slot));
-                if (w < 0) return false;
-                it = decode_item(p, w);
-                return true;
-            };
-            bool s_live = read_item(0, si, false), p_live = read_item(0, pi, true);
-            long long t0 = clock64();
-            while (ok && p_live) {
-                bool progressed = false;
-                // Issue blocks while the tensor pipe is busy (its queue is short), so
-                // the issue order is the execution order.  The order kept is
-                // P.V_j, S_{j+2}, P.V_{j+1}, ...: at most one S ahead of the next P.V,
-                // so S_{j+1} runs during the softmax of tile j and P.V_j is never
-                // queued behind two S.
-                // P.V: P and V in, and for the item's first tile O free.
-                if (tp < ts) {
-                    const int sv = tp % VSTAGES, pbuf = tp % SBUF;
-                    if (mbar_poll(bar(B_PF + pbuf), par(tp, SBUF)) && mbar_poll(bar(B_VF + sv), par(tp, VSTAGES)) &&
-                        (pj > 0 || pn < 1 || mbar_poll(bar(B_OE), par(pn - 1, 1)))) {
+        // Issue blocks while the tensor pipe is busy, so the issue order below is
+        // the execution order: per K/V tile j, P_0.V_j, S_0 of tile j+1, P_1.V_j,
+        // S_1 of tile j+1.  The softmax of one query tile thus runs while the
+        // tensor cores work on the other.
+        int t = 0;               // K/V tiles consumed
+        int c[QT] = {0, 0};      // S / P tiles per query tile
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int w = read_ring(n);
+            if (w == -2) ok = false;
+            if (w < 0) break;
+            if (lane == 0) {
+                constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
+                constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
+                const Item it = decode_item(p, w);
+                auto wait = [&](int b, uint32_t parity) {
+                    ok = ok && mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT);
+                    return ok;
+                };
+                auto issue_s = [&](int a, int qs, int kst) {
+                    const uint32_t qa = sb + OFF_Q + qs * TILE_BYTES, ka = sb + OFF_K + kst * TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
+                        mma_ss(tmem + 128u * a, smem_desc(qa + hf * HALF_BYTES + ko, 16, 1024),
+                               smem_desc(ka + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
+                    }
+                    mma_commit(bar(B_SF + a));
+                };
+                // first S of each query tile: its S columns still hold P of the
+                // previous item, whose P.V was issued before (tcgen05 runs in order)
+                if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
+                    tc_fence_after();
+                    for (int a = 0; a < QT; ++a) {
+                        const int qn = 2 * n + a, qs = qn % QSLOTS;
+                        if (it.nt[a] == 0) {
+                            mma_commit(bar(B_QE + qs));
+                            continue;
+                        }
+                        if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
                         tc_fence_after();
-                        const uint32_t vs = sb + OFF_V + sv * TILE_BYTES;
+                        issue_s(a, qs, t % KSTAGES);
+                        if (it.nt[a] == 1) mma_commit(bar(B_QE + qs));  // the tile's last S
+                    }
+                    if (ok) mma_commit(bar(B_KE + t % KSTAGES));
+                }
+                for (int j = 0; ok && j < it.nmax; ++j) {
+                    const int tv = t + j;
+                    bool v_in = false, k_in = false;
+                    for (int a = 0; a < QT; ++a) {
+                        if (j >= it.nt[a]) continue;
+                        if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
+                        if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
+                        tc_fence_after();
+                        const uint32_t va = sb + OFF_V + (tv % VSTAGES) * TILE_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + COL_O, tmem + 128u * pbuf + kk * 8,
-                                   smem_desc(vs + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (pj > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(bar(B_SE + pbuf));
-                        ++tp;
-                        if (++pj == pi.ntiles) {
-                            mma_commit(bar(B_OF));  // the item's O is complete
-                            pj = 0;
-                            ++pn;
-                            p_live = read_item(pn, pi, true);
+                            mma_ts(tmem + COL_O + 128u * a, tmem + 128u * a + kk * 8,
+                                   smem_desc(va + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                        ++c[a];
+                        if (j + 1 < it.nt[a]) {
+                            if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
+                            tc_fence_after();
+                            const int qs = (2 * n + a) % QSLOTS;
+                            issue_s(a, qs, (tv + 1) % KSTAGES);
+                            if (j + 2 == it.nt[a]) mma_commit(bar(B_QE + qs));  // the tile's last S
                         }
-                        progressed = true;
                     }
+                    if (!ok) break;
+                    mma_commit(bar(B_VE + tv % VSTAGES));
+                    if (j + 1 < it.nmax) mma_commit(bar(B_KE + (tv + 1) % KSTAGES));
                 }
-                // S: K tile in, Q of the item in, S buffer free (the P.V of the tile
-                // that last used it has completed), at most one ahead of the next P.V
-                if (s_live && ts - tp < 2) {
-                    const int st = ts % KSTAGES, sbuf = ts % SBUF, qb = sn & 1;
-                    if (mbar_poll(bar(B_KF + st), par(ts, KSTAGES)) &&
-                        (ts < SBUF || mbar_poll(bar(B_SE + sbuf), par(ts - SBUF, SBUF))) &&
-                        (sj > 0 || mbar_poll(bar(B_QF + qb), par(sn, 2)))) {
-                        tc_fence_after();
-                        const uint32_t qs = sb + OFF_Q + qb * TILE_BYTES;
-                        const uint32_t ks = sb + OFF_K + st * TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
-                            mma_ss(tmem + 128u * sbuf, smem_desc(qs + hf * HALF_BYTES + ko, 16, 1024),
-                                   smem_desc(ks + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
-                        }
-                        mma_commit(bar(B_SF + sbuf));
-                        ++ts;
-                        if (++sj == si.ntiles) {
-                            mma_commit(bar(B_QE + qb));  // the item's Q tile is no longer read
-                            sj = 0;
-                            ++sn;
-                            s_live = read_item(sn, si, false);
-                        }
-                        progressed = true;
-                    }
+                if (ok) {
+                    for (int a = 0; a < QT; ++a)
+                        if (it.nt[a] > 0) mma_commit(bar(B_OF + a));
                 }
-                if (progressed) {
-                    t0 = clock64();
-                } else if (__nanosleep(20), *abort_flag) {  // yield issue slots to the softmax warps
-                    ok = false;
-                } else if (clock64() - t0 > WAIT_LIMIT) {
-                    *abort_flag = 1;
-                    ok = false;
-                }
+                t += it.nmax;
             }
-            if (!ok) {
-                // wait for the MMAs already issued before TMEM and shared memory are released
-                volatile int32_t dummy = 0;
-                mma_commit(bar(B_DRAIN));
-                mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
-            }
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && *abort_flag) {
+            // wait for the MMAs already issued before TMEM and shared memory are released
+            volatile int32_t dummy = 0;
+            mma_commit(bar(B_DRAIN));
+            mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax + epilogue
+        const int a = (warp - 4) >> 2;  // the query tile of each item this warpgroup owns
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+        const uint32_t scol = tmem + lane_base + 128u * a;
+        const uint32_t ocol = tmem + lane_base + COL_O + 128u * a;
         const float sl2 = p.scale_log2;
-        int ts = 0;  // global tile index
+        int c = 0, no = 0, t = 0;  // tiles of this query tile, items with work, K/V tiles of all items
         bool ok = true;
         for (int n = 0;; ++n) {
-            const int slot = n % RING;
-            ok = __all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT));
-            if (!ok) break;
-            const int w = ring[slot];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+            const int w = read_ring(n);
+            if (w == -2) ok = false;
             if (w < 0) break;
             const Item it = decode_item(p, w);
-            const uint32_t ocol = tmem + lane_base + COL_O;
-            const int pos = it.offset + it.m0 + r;
-            const int last_visible = min(pos, it.kend - 1);
+            const int tbase = t;
+            t += it.nmax;
+            if (it.nt[a] == 0) continue;
+            // rows past the last visible key of the item's last K/V tile may be
+            // unused pool slots (any bits): the warpgroup of the first query tile
+            // that reads that tile sets those V rows to 0 so that 0 * V stays 0
+            const bool zeroer = paged && a == (it.nt[0] == it.nmax ? 0 : 1) && it.kend_max < it.nmax * BN;
+            const int pos = it.offset + it.m0[a] + r;
+            const int last_visible = min(pos, it.kend[a] - 1);
             float m_used = -INFINITY;  // running max in scaled base-2 units
             float l = 0.f;
-            for (int j = 0; j < it.ntiles; ++j, ++ts) {
-                const int sbuf = ts % SBUF;
-                ok = __all_sync(FULL, mbar_wait(bar(B_SF + sbuf), par(ts, SBUF), abort_flag, WAIT_LIMIT));
+            for (int j = 0; j < it.nt[a]; ++j, ++c) {
+                ok = __all_sync(FULL, mbar_wait(bar(B_SF + a), uint32_t(c) & 1u, abort_flag, WAIT_LIMIT));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t scol = tmem + lane_base + 128u * sbuf;
                 const int j0 = j * BN;
-                const bool masked = j0 + BN - 1 > it.offset + it.m0;  // the tile crosses some row's causal bound
+                const bool masked = j0 + BN - 1 > it.offset + it.m0[a];  // the tile crosses some row's causal bound
                 const int limit = last_visible - j0;
                 // pass 1: row max of the raw scores
                 float mx8[8];
@@ -547,10 +594,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     tmem_ld64_sync(scol + hf * 64, sr);
                     if (masked) mask_tail(sr, hf * 64, limit);
 #pragma unroll
-                    for (int c = 0; c < 64; c += 16) {
+                    for (int cc = 0; cc < 64; cc += 16) {
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mx8[k] = fmax3(mx8[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+                            mx8[k] = fmax3(mx8[k], __uint_as_float(sr[cc + k]), __uint_as_float(sr[cc + 8 + k]));
                     }
                 }
                 const float mx =
@@ -559,12 +606,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 const float m_new = need ? mx : m_used;
                 const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
                 if (j > 0 && __any_sync(FULL, need)) {
-                    // O must hold the previous tile's P.V before it is rescaled; the
-                    // free barrier of that tile's S buffer tracks its completion
-                    ok = __all_sync(FULL, mbar_wait(bar(B_SE + (ts - 1) % SBUF), par(ts - 1, SBUF), abort_flag,
-                                                    WAIT_LIMIT));
-                    if (!ok) break;
-                    tc_fence_after();
+                    // O holds the previous tile's P.V: that P.V was issued before this
+                    // tile's S, whose completion the S barrier reports
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint32_t o[32];
@@ -597,44 +640,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     tmem_st32_sync(scol + hf * 32, pk);
                 }
                 l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-                if (paged && j == it.ntiles - 1 && it.kend < j0 + BN) {
-                    // rows past the last visible key may be unused pool slots (any bits): make them 0
-                    // so that 0 * V stays 0 in P.V
-                    const int sv = ts % VSTAGES;
-                    ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), par(ts, VSTAGES), abort_flag, WAIT_LIMIT));
+                if (zeroer && j == it.nmax - 1) {
+                    const int tv = tbase + j, sv = tv % VSTAGES;
+                    ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), par(tv, VSTAGES), abort_flag, WAIT_LIMIT));
                     if (!ok) break;
-                    if (j0 + r >= it.kend) {
+                    if (j0 + r >= it.kend_max) {
                         uint4 *row0 = reinterpret_cast<uint4 *>(smem + OFF_V + sv * TILE_BYTES + r * 128);
                         uint4 *row1 = reinterpret_cast<uint4 *>(smem + OFF_V + sv * TILE_BYTES + HALF_BYTES + r * 128);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) row0[c] = row1[c] = make_uint4(0, 0, 0, 0);
+                        for (int cc = 0; cc < 8; ++cc) row0[cc] = row1[cc] = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                mbar_arrive(bar(B_PF + sbuf));
+                mbar_arrive(bar(B_PF + a));
             }
             if (!ok) break;
-            // epilogue: O is complete once its own barrier fires (a single-use
-            // phase per item); read it all, hand it back, then normalise and store
-            ok = __all_sync(FULL, mbar_wait(bar(B_OF), par(n, 1), abort_flag, WAIT_LIMIT));
+            // epilogue: the item's O of this query tile is complete once its barrier
+            // fires; the next item's first P.V (which overwrites O) waits for this
+            // warpgroup's next P, written after these reads
+            ok = __all_sync(FULL, mbar_wait(bar(B_OF + a), uint32_t(no) & 1u, abort_flag, WAIT_LIMIT));
+            ++no;
             if (!ok) break;
             tc_fence_after();
-            uint32_t o[128];
-            tmem_ld128_sync(ocol, o);
-            tc_fence_before();
-            mbar_arrive(bar(B_OE));  // the next item's P.V may overwrite O now
             const float inv = 1.f / l;
-            if (r < it.rows) {
-                uint4 *d4 = reinterpret_cast<uint4 *>(p.out + (int64_t(it.q0 + it.m0 + r) * p.num_heads + it.h) * D);
 #pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    uint4 u;
-                    u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                    u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                    u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                    u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                    d4[v] = u;
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t o[64];
+                tmem_ld64_sync(ocol + hf * 64, o);
+                if (r < it.rows[a]) {
+                    uint4 *d4 =
+                        reinterpret_cast<uint4 *>(p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint4 u;
+                        u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                        u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                        u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                        u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                        d4[hf * 8 + v] = u;
+                    }
                 }
             }
         }
@@ -737,6 +782,9 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
     p.cu_k = cu_seqlens_k;
     p.max_q = max_seqlen_q;
     p.n_mtiles = (max_seqlen_q + BM - 1) / BM;
+    p.pair_heads = num_heads / num_kv_heads >= 2 ? 1 : 0;
+    p.n_steps = p.pair_heads ? p.n_mtiles : (p.n_mtiles + 1) / 2;
+    p.units = p.pair_heads ? num_heads / 2 : num_heads;
     p.num_heads = num_heads;
     p.num_seqs = num_seqs;
     p.kv_heads = num_kv_heads;
@@ -757,7 +805,7 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
         attr_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    const int64_t items = int64_t(p.n_mtiles) * num_heads * num_seqs;
+    const int64_t items = int64_t(p.n_steps) * p.units * num_seqs;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
     const dim3 grid(unsigned(items < sms ? items : sms));
     prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(p);

@@ -266,6 +266,26 @@ __device__ __forceinline__ void tmem_st64_sync(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
+// ------------------------------------------------------------------ registers
+
+// Move registers between the warpgroups of a CTA: every warp of a warpgroup
+// executes the same call.  A decrease returns registers to the CTA's pool, an
+// increase waits until the pool holds enough (the pool is what the CTA was
+// launched with, threads x registers per thread).
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease()
+{
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase()
+{
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ math
 
 __device__ __forceinline__ float ex2_approx(float x)
