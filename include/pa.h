@@ -100,7 +100,11 @@ pa_status pa_store_kvcache(const void *k, int64_t k_stride_tok, const void *v, i
  * head h reads KV head h / (num_heads / num_kv_heads).
  *
  *   q             [Tq, num_heads, head_dim] bf16, token stride q_stride_tok
- *                 elements; Tq = cu_seqlens_q[num_seqs].
+ *                 elements (a multiple of 8); Tq = cu_seqlens_q[num_seqs].
+ *   num_tokens    rows q holds (and, without a table, k and v hold): at
+ *                 least Tq.  The kernel reads no row at or past it; a
+ *                 sequence whose rows would pass it sets PA_ERR_INVALID_ARG
+ *                 and is skipped.  0 launches nothing.
  *   block_table   NULL: keys come from k / v rows cu_seqlens_k[b] ..
  *                 (token stride kv_stride_tok), which requires
  *                 cu_seqlens_k == cu_seqlens_q (checked on the device:
@@ -119,7 +123,7 @@ pa_status pa_store_kvcache(const void *k, int64_t k_stride_tok, const void *v, i
  *   out           [Tq, num_heads, head_dim] bf16, packed.
  * Sequences with Lq_b == 0 are skipped.  Lk_b < Lq_b sets PA_ERR_INVALID_ARG.
  */
-pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok,
+pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64_t num_tokens,
                            const void *k, const void *v, int64_t kv_stride_tok,
                            const void *k_cache, const void *v_cache, int64_t num_blocks, int block_size,
                            const int32_t *block_table, int max_blocks_per_seq,

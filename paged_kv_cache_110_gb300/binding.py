@@ -45,7 +45,7 @@ def _load() -> ctypes.CDLL:
     L.pa_store_kvcache.restype = i32
     L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
     L.pa_prefill_paged.restype = i32
-    L.pa_prefill_paged.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32,
+    L.pa_prefill_paged.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32,
                                    i32, i32, i32, f32, vp, vp, vp]
     L.pa_decode_workspace_bytes.restype = sz
     L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -145,6 +145,8 @@ def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
         _, vs = _bf16_rows(v, "v")
         if vs != kvs:
             raise ValueError("k and v must share a token stride")
+        if k.shape[0] < q.shape[0] or v.shape[0] < q.shape[0]:
+            raise ValueError("k and v need a row per query token")
         args = (_ptr(k), _ptr(v), kvs, None, None, 0, 16, None, 1)
     else:
         nb, bs, hkv, _ = _cache(k_cache, "k_cache")
@@ -153,7 +155,7 @@ def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
         if block_table.dim() != 2 or block_table.shape[0] != nseq:
             raise ValueError("block_table must be [num_seqs, max_blocks]")
         args = (None, None, 0, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table), block_table.shape[1])
-    _check(lib.pa_prefill_paged(_ptr(q), qs, *args, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
+    _check(lib.pa_prefill_paged(_ptr(q), qs, q.shape[0], *args, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
                                 int(max_seqlen_q), int(max_seqlen_k), hq, hkv, q.shape[2], float(scale), _ptr(out),
                                 _ptr(dev_status), _stream(stream)),
            "pa_prefill_paged")

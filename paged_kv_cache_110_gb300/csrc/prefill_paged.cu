@@ -16,15 +16,18 @@
 // Each K and V tile is loaded once for both, and while one tile's softmax runs
 // the tensor cores work on the other's, so the two dependency chains
 // (S -> softmax -> P.V) hide each other.
-//   warp 3      scheduler: fetches items, publishes them in a ring of 4,
-//               stages each item's block ids (validated) and loads its two Q
-//               tiles (cp.async, rows past the sequence zero-filled) into a
-//               ring of three Q buffers.
+//   warp 3      scheduler: fetches items, decodes each once and publishes it
+//               in a ring of 4, stages its block ids (validated) and loads its
+//               two Q tiles by TMA into a ring of three Q buffers.
 //   warp 0      K producer, warp 2 V producer: paged tiles arrive by TMA, one
 //               box per page run (box height gcd(block_size, 128) rows, so a
-//               box never crosses a page); without a table rows are copied with
-//               cp.async.  Tiles land in shared memory in the 128-byte-swizzled
-//               layout the tensor cores read; two stages each.
+//               box never crosses a page); without a table one box of 128
+//               token rows.  Tiles land in shared memory in the
+//               128-byte-swizzled layout the tensor cores read; two stages
+//               each.  Rows a tile holds beyond a sequence (the next
+//               sequence's rows, TMA zero fill, unused pool slots) are masked
+//               out of S, and the V rows of the item's last tile past its last
+//               key are set to zero before P.V, so that they add 0.
 //   warp 1      MMA issuer (one thread): per K/V tile j, O_0 += P_0 V_j then
 //               S_0 = Q_0 K_{j+1}^T, then the same for query tile 1.  S and O of
 //               each query tile live in TMEM (S at columns 0 / 128, O at
@@ -62,8 +65,8 @@ constexpr int VSTAGES = 2;          // V tiles in flight
 constexpr int QSLOTS = 3;           // Q tile buffers: one item's pair and the next item's first tile
 constexpr int RING = 4;             // work items fetched ahead by the scheduler warp
 constexpr int NTHREADS = 384;
-constexpr uint32_t REGS_CONTROL = 96;   // per thread, warps 0-3 (one warpgroup)
-constexpr uint32_t REGS_SOFTMAX = 200;  // per thread, warps 4-11
+constexpr uint32_t REGS_CONTROL = 136;  // per thread, warps 0-3 (one warpgroup)
+constexpr uint32_t REGS_SOFTMAX = 184;  // per thread, warps 4-11
 constexpr int HALF_BYTES = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte swizzle column block)
 constexpr int TILE_BYTES = 2 * HALF_BYTES;  // 128 rows x 128 bf16
 constexpr int OFF_Q = 0;
@@ -71,7 +74,7 @@ constexpr int OFF_K = OFF_Q + QSLOTS * TILE_BYTES;
 constexpr int OFF_V = OFF_K + KSTAGES * TILE_BYTES;
 constexpr int OFF_BAR = OFF_V + VSTAGES * TILE_BYTES;
 enum {
-    B_QF = 0,                    // Q buffer loaded (32 arrivals)
+    B_QF = 0,                    // Q buffer loaded (TMA transaction bytes)
     B_QE = B_QF + QSLOTS,        // Q buffer free (its tile's last S done)
     B_KF = B_QE + QSLOTS,        // K stage loaded
     B_KE = B_KF + KSTAGES,       // K stage free (every S reading it done)
@@ -88,9 +91,11 @@ enum {
     NBAR = B_DRAIN + 1
 };
 constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA thread, softmax warps
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag, item ring
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag
+constexpr int OFF_RING = OFF_MISC + 16;           // the item ring (RingSlot x RING)
+constexpr int RING_SLOT_BYTES = 80;
 constexpr int TABLE_SMEM = 256;                   // block ids staged per item (more: read from global)
-constexpr int OFF_TABLE = OFF_MISC + 32;          // two buffers
+constexpr int OFF_TABLE = OFF_RING + RING * RING_SLOT_BYTES;  // two buffers
 constexpr int SMEM_BYTES = OFF_TABLE + 2 * TABLE_SMEM * 4;  // the base is 1024-byte aligned (checked)
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;                  // S of tiles 0 / 1 at 0 / 128, O at 256 / 384
@@ -102,13 +107,10 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr uint32_t NEG_INF_BITS = 0xff800000u;
 
 struct TcParams {
-    CUtensorMap kmap;  // paged pool, [num_blocks * block_size rows, Hkv * 128 cols]
+    CUtensorMap qmap;  // [num_tokens rows, Hq * 128 cols]
+    CUtensorMap kmap;  // paged pool [num_blocks * block_size rows, Hkv * 128 cols], or k [num_tokens rows, ...]
     CUtensorMap vmap;
-    const uint16_t *q;
-    int64_t q_stride;
-    const uint16_t *k;  // no-table path
-    const uint16_t *v;
-    int64_t kv_stride;
+    int64_t num_tokens;
     const int32_t *block_table;
     int max_blocks;
     int block_size;
@@ -138,11 +140,6 @@ struct TcParams {
 constexpr unsigned SCHED_SLOTS = 4096;
 __device__ unsigned int g_prefill_sched[SCHED_SLOTS][2];
 
-__device__ __forceinline__ uint32_t swz128(int row, int chunk)  // byte offset in a 128-row, 128-byte-row block
-{
-    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 // Parity of completion number n of a barrier used by every nbuf-th round.
 __device__ __forceinline__ uint32_t par(int n, int nbuf) { return uint32_t(n / nbuf) & 1u; }
 
@@ -171,9 +168,10 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
     it.k0 = p.cu_k[it.b];
     const int lk = p.cu_k[it.b + 1] - it.k0;
     const bool paged = p.block_table != nullptr;
-    it.bad = lk < lq || (!paged && (lk != lq || it.k0 != it.q0)) ||
+    const bool rows_out = it.q0 < 0 || lq < 0 || int64_t(it.q0) + lq > p.num_tokens;
+    it.bad = lk < lq || rows_out || (!paged && (lk != lq || it.k0 != it.q0)) ||
              (paged && int64_t(lk) > int64_t(p.max_blocks) * p.block_size);
-    it.bad_code = (lk < lq || !paged) ? PA_ERR_INVALID_ARG : PA_ERR_BOUNDS;
+    it.bad_code = (lk < lq || rows_out || !paged) ? PA_ERR_INVALID_ARG : PA_ERR_BOUNDS;
     it.offset = lk - lq;
     // rows beyond the stated maximum are not computed (the call reports it)
     const int lq_c = min(lq, p.max_q);
@@ -199,27 +197,39 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
     return it;
 }
 
+// An item as the scheduler publishes it (w = -1 ends the stream).
+struct RingSlot {
+    int w;
+    Item it;
+};
+static_assert(sizeof(RingSlot) <= RING_SLOT_BYTES, "ring slot size");
+
 // Where one producer warp reads a tile from: the TMA map of the paged pool
-// (with the item's block ids; -1 marks an id that failed validation), or the
-// new-token rows when there is no table.
+// with the item's block ids (-1 marks an id that failed validation), or, when
+// there is no table, the map of the new-token rows from row0 on.
 struct TileSource {
-    const CUtensorMap *map;  // paged
+    const CUtensorMap *map;
     const int32_t *table;    // paged
     int box_rows;
     int block_size;
-    const uint16_t *rows;    // no table: first row of the sequence, head g
-    int64_t stride;          // no table: row stride in elements
-    const uint16_t *dummy;   // any mapped address (zero-byte cp.async source)
+    int row0;                // no table: the sequence's first token row
 };
 
 // Issue the loads of the 128-key tile starting at key j0 into `dst`,
-// arriving on `bar`.  Paged: lane 0 issues one TMA box per page run; boxes
-// at or past kend and boxes on invalid ids are skipped.  No table: the 32
-// lanes copy rows with cp.async (rows past kend zero-filled) and then arrive.
+// arriving on `bar` (lane 0 issues).  Paged: one TMA box per page run; boxes
+// at or past kend and boxes on invalid ids are skipped.  No table: one box of
+// 128 token rows (rows past the last token are zero-filled by TMA).
 __device__ __forceinline__ void load_tile(const TileSource &src, int xcol, int j0, int kend, uint32_t dst,
                                           uint32_t bar, int lane, int64_t num_blocks)
 {
-    if (src.map != nullptr) {
+    if (src.table == nullptr) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, TILE_BYTES);
+            tma_load_2d(dst, src.map, xcol, src.row0 + j0, bar);
+            tma_load_2d(dst + HALF_BYTES, src.map, xcol + 64, src.row0 + j0, bar);
+        }
+        __syncwarp();
+    } else {
         if (lane == 0) {
             const int nbox = BN / src.box_rows;
             uint32_t bytes = 0;
@@ -242,16 +252,6 @@ __device__ __forceinline__ void load_tile(const TileSource &src, int xcol, int j
             }
         }
         __syncwarp();
-    } else {
-        for (int idx = lane; idx < BN * 16; idx += 32) {
-            const int r = idx >> 4, c = idx & 15;
-            const bool valid = j0 + r < kend;
-            const uint16_t *ptr = valid ? src.rows + int64_t(j0 + r) * src.stride + c * 8 : src.dummy;
-            cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7), ptr, valid);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(bar);
     }
 }
 
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const uint32_t sb = smem_u32(smem);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 4);
-    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + OFF_MISC + 16);
+    RingSlot *ring = reinterpret_cast<RingSlot *>(smem + OFF_RING);
     auto bar = [&](int i) { return sb + OFF_BAR + 8u * uint32_t(i); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the 128-byte swizzle pattern of TMA and the tensor cores is anchored at 1024-byte boundaries
@@ -283,17 +283,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const int n_items = p.n_steps * p.units * p.num_seqs;
 
     if (threadIdx.x == 0) {
-        const uint32_t loader_count = paged ? 1 : 32;
         for (int s = 0; s < QSLOTS; ++s) {
-            mbar_init(bar(B_QF + s), 32);
+            mbar_init(bar(B_QF + s), 1);
             mbar_init(bar(B_QE + s), 1);
         }
         for (int s = 0; s < KSTAGES; ++s) {
-            mbar_init(bar(B_KF + s), loader_count);
+            mbar_init(bar(B_KF + s), 1);
             mbar_init(bar(B_KE + s), 1);
         }
         for (int s = 0; s < VSTAGES; ++s) {
-            mbar_init(bar(B_VF + s), loader_count);
+            mbar_init(bar(B_VF + s), 1);
             mbar_init(bar(B_VE + s), 1);
         }
         for (int a = 0; a < QT; ++a) {
@@ -331,10 +330,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
     // Read item n from the ring (every lane of the calling warp waits; lane 0
     // releases the slot).  Returns the item number, -1 at the end, -2 on abort.
-    auto read_ring = [&](int n) -> int {
+    auto read_ring = [&](int n, Item &it) -> int {
         const int slot = n % RING;
         if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) return -2;
-        const int w = ring[slot];
+        const int w = ring[slot].w;
+        if (w >= 0) it = ring[slot].it;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_IRE + slot));
         return w;
@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // Fetch work items from the call's counter (heaviest first), publish each
         // in the item ring, stage its block ids (validated) for the producers and
         // load its two Q tiles.
+        if (lane == 0) tma_prefetch_desc(&p.qmap);
         int n = 0;  // items published
         while (true) {
             int w = -1;
@@ -387,12 +388,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 mbar_arrive(bar(B_TF + tb));
             }
             if (lane == 0) {
-                ring[slot] = w;
+                ring[slot].w = w;
+                if (w >= 0) ring[slot].it = it;
                 mbar_arrive(bar(B_IRF + slot));
             }
             if (w < 0) break;
-            // the item's Q tiles (rows past the sequence zero-filled) into Q buffers
-            // 2n and 2n+1 of the ring of three
+            // the item's Q tiles into Q buffers 2n and 2n+1 of the ring of three
+            // (rows past the sequence are other sequences' rows or TMA zero fill:
+            // their results are not stored)
             bool ok = true;
             for (int a = 0; a < QT && ok; ++a) {
                 const int qn = 2 * n + a, qs = qn % QSLOTS;
@@ -400,19 +403,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     !(ok = __all_sync(FULL, mbar_wait(bar(B_QE + qs), par(qn - QSLOTS, QSLOTS), abort_flag,
                                                       WAIT_LIMIT))))
                     break;
-                if (it.rows[a] > 0) {
-                    const uint32_t dst = sb + OFF_Q + qs * TILE_BYTES;
-                    const uint16_t *src = p.q + int64_t(it.q0 + it.m0[a]) * p.q_stride + it.h[a] * D;
-                    for (int idx = lane; idx < BM * 16; idx += 32) {
-                        const int r = idx >> 4, c = idx & 15;
-                        const bool valid = r < it.rows[a];
-                        cp_async16(dst + (c >> 3) * HALF_BYTES + swz128(r, c & 7),
-                                   valid ? src + int64_t(r) * p.q_stride + c * 8 : p.q, valid);
+                if (lane == 0) {
+                    if (it.rows[a] > 0) {
+                        const uint32_t dst = sb + OFF_Q + qs * TILE_BYTES, qb = bar(B_QF + qs);
+                        mbar_arrive_expect_tx(qb, TILE_BYTES);
+                        tma_load_2d(dst, &p.qmap, it.h[a] * D, it.q0 + it.m0[a], qb);
+                        tma_load_2d(dst + HALF_BYTES, &p.qmap, it.h[a] * D + 64, it.q0 + it.m0[a], qb);
+                    } else {
+                        mbar_arrive(bar(B_QF + qs));
                     }
-                    cp_async_wait_all();
-                    fence_proxy_async_smem();
                 }
-                mbar_arrive(bar(B_QF + qs));
+                __syncwarp();
             }
             if (!ok) break;
             ++n;
@@ -421,12 +422,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // ------------------------------------------------------------ producers (K, V)
         const bool is_k = warp == 0;
         TileSource src;
-        src.map = paged ? (is_k ? &p.kmap : &p.vmap) : nullptr;
+        src.map = is_k ? &p.kmap : &p.vmap;
         src.box_rows = p.box_rows;
         src.block_size = p.block_size;
-        src.stride = p.kv_stride;
-        src.dummy = p.q;
-        if (paged && lane == 0) tma_prefetch_desc(src.map);
+        if (lane == 0) tma_prefetch_desc(src.map);
         constexpr int nst = KSTAGES;
         static_assert(KSTAGES == VSTAGES, "one stage count for both producers");
         const uint32_t base = sb + (is_k ? OFF_K : OFF_V);
@@ -434,17 +433,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         int t = 0;  // tiles issued
         bool ok = true;
         for (int n = 0;; ++n) {
-            const int w = read_ring(n);
+            Item it;
+            const int w = read_ring(n, it);
             if (w == -2) ok = false;
             if (w < 0) break;
-            const Item it = decode_item(p, w);
             const int tb = n & 1;
             if (!(ok = mbar_wait(bar(B_TF + tb), par(n, 2), abort_flag, WAIT_LIMIT))) break;
             const int nblk = paged ? (it.kend_max + p.block_size - 1) / p.block_size : 0;
             src.table = (paged && nblk <= TABLE_SMEM)
                             ? reinterpret_cast<const int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM
                             : (paged ? p.block_table + int64_t(it.b) * p.max_blocks : nullptr);
-            src.rows = paged ? nullptr : (is_k ? p.k : p.v) + int64_t(it.k0) * p.kv_stride + it.g * D;
+            src.row0 = it.k0;
             for (int j = 0; j < it.nmax; ++j, ++t) {
                 const int st = t % nst;
                 if (t >= nst && !(ok = mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, WAIT_LIMIT)))
@@ -455,7 +454,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             if (!ok) break;
             if (lane == 0) mbar_arrive(bar(B_TE + tb));  // this producer no longer reads the block ids
         }
-        if (*abort_flag && paged && lane == 0) {
+        if (*abort_flag && lane == 0) {
             // let copies already in flight land before the CTA's shared memory goes away
             volatile int32_t dummy = 0;
             for (int u = max(0, t - nst); u < t; ++u)
@@ -471,13 +470,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         int c[QT] = {0, 0};      // S / P tiles per query tile
         bool ok = true;
         for (int n = 0; ok; ++n) {
-            const int w = read_ring(n);
+            Item it;
+            const int w = read_ring(n, it);
             if (w == -2) ok = false;
             if (w < 0) break;
             if (lane == 0) {
                 constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
                 constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
-                const Item it = decode_item(p, w);
                 auto wait = [&](int b, uint32_t parity) {
                     ok = ok && mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT);
                     return ok;
@@ -562,17 +561,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         int c = 0, no = 0, t = 0;  // tiles of this query tile, items with work, K/V tiles of all items
         bool ok = true;
         for (int n = 0;; ++n) {
-            const int w = read_ring(n);
+            Item it;
+            const int w = read_ring(n, it);
             if (w == -2) ok = false;
             if (w < 0) break;
-            const Item it = decode_item(p, w);
             const int tbase = t;
             t += it.nmax;
             if (it.nt[a] == 0) continue;
-            // rows past the last visible key of the item's last K/V tile may be
-            // unused pool slots (any bits): the warpgroup of the first query tile
-            // that reads that tile sets those V rows to 0 so that 0 * V stays 0
-            const bool zeroer = paged && a == (it.nt[0] == it.nmax ? 0 : 1) && it.kend_max < it.nmax * BN;
+            // rows past the last key of the item's last K/V tile may be unused
+            // pool slots (any bits) or another sequence's rows: the warpgroup of
+            // the first query tile that reads that tile sets those V rows to 0
+            // so that 0 * V stays 0
+            const bool zeroer = a == (it.nt[0] == it.nmax ? 0 : 1) && it.kend_max < it.nmax * BN;
             const int pos = it.offset + it.m0[a] + r;
             const int last_visible = min(pos, it.kend[a] - 1);
             float m_used = -INFINITY;  // running max in scaled base-2 units
@@ -718,12 +718,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-bool make_pool_map(CUtensorMap *map, const void *base, int64_t rows, int kv_heads, int box_rows)
+// A 2-D map over `rows` rows of `heads` * 128 bf16 each, rows `stride`
+// elements apart, read in boxes of 64 columns x box_rows rows with the
+// 128-byte swizzle.
+bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int64_t stride, int box_rows)
 {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {cuuint64_t(kv_heads) * D, cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(kv_heads) * D * 2};
+    const cuuint64_t dims[2] = {cuuint64_t(heads) * D, cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(stride) * 2};
     const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -735,7 +738,8 @@ int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
 
 }  // namespace
 
-extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const void *k, const void *v,
+extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64_t num_tokens, const void *k,
+                                      const void *v,
                                       int64_t kv_stride_tok, const void *k_cache, const void *v_cache,
                                       int64_t num_blocks, int block_size, const int32_t *block_table,
                                       int max_blocks_per_seq, const int32_t *cu_seqlens_q,
@@ -743,13 +747,15 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
                                       int max_seqlen_k, int num_heads, int num_kv_heads, int head_dim,
                                       float scale, void *out, int32_t *dev_status, void *stream)
 {
-    if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_blocks < 0 || num_tokens < 0)
+        return PA_ERR_INVALID_ARG;
     if (head_dim != D || !pa::pow2_in(num_kv_heads, 1, 8) || num_heads <= 0 || num_heads % num_kv_heads != 0 ||
         !pa::pow2_in(num_heads / num_kv_heads, 1, 8))
         return PA_ERR_UNSUPPORTED;
     if (block_table != nullptr && (block_size < 16 || block_size > 1024 || block_size % 16 != 0))
         return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || max_seqlen_q == 0) return PA_OK;
+    if (num_seqs == 0 || max_seqlen_q == 0 || num_tokens == 0) return PA_OK;
+    if (num_tokens >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
     if (!q || !cu_seqlens_q || !cu_seqlens_k || !out) return PA_ERR_INVALID_ARG;
     if (q_stride_tok < int64_t(num_heads) * D || q_stride_tok % 8 != 0 || !pa::aligned(q, 16))
         return PA_ERR_INVALID_ARG;
@@ -768,11 +774,7 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
 
     TcParams p;
     memset(&p, 0, sizeof(p));
-    p.q = static_cast<const uint16_t *>(q);
-    p.q_stride = q_stride_tok;
-    p.k = static_cast<const uint16_t *>(k);
-    p.v = static_cast<const uint16_t *>(v);
-    p.kv_stride = kv_stride_tok;
+    p.num_tokens = num_tokens;
     p.block_table = block_table;
     p.max_blocks = max_blocks_per_seq;
     p.block_size = block_size;
@@ -793,10 +795,15 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, const
     p.status = dev_status;
     static std::atomic<unsigned> next_slot{0};
     p.sched_slot = next_slot.fetch_add(1u, std::memory_order_relaxed) % SCHED_SLOTS;
+    if (!make_rows_map(&p.qmap, q, num_tokens, num_heads, q_stride_tok, BM)) return PA_ERR_CUDA;
     if (block_table != nullptr) {
-        const int64_t rows = num_blocks * block_size;
-        if (!make_pool_map(&p.kmap, k_cache, rows, num_kv_heads, p.box_rows) ||
-            !make_pool_map(&p.vmap, v_cache, rows, num_kv_heads, p.box_rows))
+        const int64_t rows = num_blocks * block_size, row = int64_t(num_kv_heads) * D;
+        if (!make_rows_map(&p.kmap, k_cache, rows, num_kv_heads, row, p.box_rows) ||
+            !make_rows_map(&p.vmap, v_cache, rows, num_kv_heads, row, p.box_rows))
+            return PA_ERR_CUDA;
+    } else {
+        if (!make_rows_map(&p.kmap, k, num_tokens, num_kv_heads, kv_stride_tok, BN) ||
+            !make_rows_map(&p.vmap, v, num_tokens, num_kv_heads, kv_stride_tok, BN))
             return PA_ERR_CUDA;
     }
     static std::once_flag attr_once;

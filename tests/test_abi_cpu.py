@@ -80,10 +80,10 @@ def test_store_host_checks(lib):
 def test_prefill_host_checks(lib):
     f = lib.pa_prefill_paged
 
-    def call(q=FAKE, qs=2048, k=None, v=None, kvs=0, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2, cuq=FAKE,
-             cuk=FAKE, ns=2, mq=8, mk=8, hq=16, hkv=8, d=128, out=FAKE):
-        return f(q, qs, k, v, kvs, kc, vc, nb, bs, bt, mb, cuq, cuk, ns, mq, mk, hq, hkv, d, ctypes.c_float(0.1),
-                 out, None, None)
+    def call(q=FAKE, qs=2048, nt=16, k=None, v=None, kvs=0, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2,
+             cuq=FAKE, cuk=FAKE, ns=2, mq=8, mk=8, hq=16, hkv=8, d=128, out=FAKE):
+        return f(q, qs, nt, k, v, kvs, kc, vc, nb, bs, bt, mb, cuq, cuk, ns, mq, mk, hq, hkv, d,
+                 ctypes.c_float(0.1), out, None, None)
 
     assert call(d=64) == 2
     assert call(hq=12, hkv=8) == 2
@@ -94,6 +94,9 @@ def test_prefill_host_checks(lib):
     assert call(bt=None) == 1                               # no table and no k / v
     assert call(bt=None, k=FAKE, v=FAKE, kvs=1024, mk=9) == 1  # null table needs max_seqlen_k == max_seqlen_q
     assert call(qs=100) == 1
+    assert call(nt=-1) == 1
+    assert call(nt=0) == 0                                  # no query rows: nothing to do
+    assert call(nt=1 << 31) == 2
 
 
 def test_decode_host_checks(lib):
