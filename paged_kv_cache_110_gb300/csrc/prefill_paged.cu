@@ -465,88 +465,92 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // Issue blocks while the tensor pipe is busy, so the issue order below is
         // the execution order: per K/V tile j, P_0.V_j, S_0 of tile j+1, P_1.V_j,
         // S_1 of tile j+1.  The softmax of one query tile thus runs while the
-        // tensor cores work on the other.
-        int t = 0;               // K/V tiles consumed
-        int c[QT] = {0, 0};      // S / P tiles per query tile
-        bool ok = true;
-        for (int n = 0; ok; ++n) {
-            Item it;
-            const int w = read_ring(n, it);
-            if (w == -2) ok = false;
-            if (w < 0) break;
-            if (lane == 0) {
-                constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
-                constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
-                auto wait = [&](int b, uint32_t parity) {
-                    ok = ok && mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT);
-                    return ok;
-                };
-                auto issue_s = [&](int a, int qs, int kst) {
-                    const uint32_t qa = sb + OFF_Q + qs * TILE_BYTES, ka = sb + OFF_K + kst * TILE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
-                        mma_ss(tmem + 128u * a, smem_desc(qa + hf * HALF_BYTES + ko, 16, 1024),
-                               smem_desc(ka + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
-                    }
-                    mma_commit(bar(B_SF + a));
-                };
-                // first S of each query tile: its S columns still hold P of the
-                // previous item, whose P.V was issued before (tcgen05 runs in order)
-                if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
-                    tc_fence_after();
-                    for (int a = 0; a < QT; ++a) {
-                        const int qn = 2 * n + a, qs = qn % QSLOTS;
-                        if (it.nt[a] == 0) {
-                            mma_commit(bar(B_QE + qs));
-                            continue;
+        // tensor cores work on the other.  One thread runs this role; the
+        // warp's other lanes wait at the end.
+        if (lane == 0) {
+            int t = 0;               // K/V tiles consumed
+            int c[QT] = {0, 0};      // S / P tiles per query tile
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % RING;
+                if (!mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT)) break;
+                const int w = ring[slot].w;
+                if (w < 0) break;
+                const Item it = ring[slot].it;
+                mbar_arrive(bar(B_IRE + slot));
+                {
+                    constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
+                    constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
+                    auto wait = [&](int b, uint32_t parity) {
+                        ok = ok && mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT);
+                        return ok;
+                    };
+                    auto issue_s = [&](int a, int qs, int kst) {
+                        const uint32_t qa = sb + OFF_Q + qs * TILE_BYTES, ka = sb + OFF_K + kst * TILE_BYTES;
+    #pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
+                            mma_ss(tmem + 128u * a, smem_desc(qa + hf * HALF_BYTES + ko, 16, 1024),
+                                   smem_desc(ka + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
                         }
-                        if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
+                        mma_commit(bar(B_SF + a));
+                    };
+                    // first S of each query tile: its S columns still hold P of the
+                    // previous item, whose P.V was issued before (tcgen05 runs in order)
+                    if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
                         tc_fence_after();
-                        issue_s(a, qs, t % KSTAGES);
-                        if (it.nt[a] == 1) mma_commit(bar(B_QE + qs));  // the tile's last S
-                    }
-                    if (ok) mma_commit(bar(B_KE + t % KSTAGES));
-                }
-                for (int j = 0; ok && j < it.nmax; ++j) {
-                    const int tv = t + j;
-                    bool v_in = false, k_in = false;
-                    for (int a = 0; a < QT; ++a) {
-                        if (j >= it.nt[a]) continue;
-                        if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
-                        if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
-                        tc_fence_after();
-                        const uint32_t va = sb + OFF_V + (tv % VSTAGES) * TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + COL_O + 128u * a, tmem + 128u * a + kk * 8,
-                                   smem_desc(va + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                        ++c[a];
-                        if (j + 1 < it.nt[a]) {
-                            if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
+                        for (int a = 0; a < QT; ++a) {
+                            const int qn = 2 * n + a, qs = qn % QSLOTS;
+                            if (it.nt[a] == 0) {
+                                mma_commit(bar(B_QE + qs));
+                                continue;
+                            }
+                            if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
                             tc_fence_after();
-                            const int qs = (2 * n + a) % QSLOTS;
-                            issue_s(a, qs, (tv + 1) % KSTAGES);
-                            if (j + 2 == it.nt[a]) mma_commit(bar(B_QE + qs));  // the tile's last S
+                            issue_s(a, qs, t % KSTAGES);
+                            if (it.nt[a] == 1) mma_commit(bar(B_QE + qs));  // the tile's last S
                         }
+                        if (ok) mma_commit(bar(B_KE + t % KSTAGES));
                     }
-                    if (!ok) break;
-                    mma_commit(bar(B_VE + tv % VSTAGES));
-                    if (j + 1 < it.nmax) mma_commit(bar(B_KE + (tv + 1) % KSTAGES));
+                    for (int j = 0; ok && j < it.nmax; ++j) {
+                        const int tv = t + j;
+                        bool v_in = false, k_in = false;
+                        for (int a = 0; a < QT; ++a) {
+                            if (j >= it.nt[a]) continue;
+                            if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
+                            if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
+                            tc_fence_after();
+                            const uint32_t va = sb + OFF_V + (tv % VSTAGES) * TILE_BYTES;
+    #pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                mma_ts(tmem + COL_O + 128u * a, tmem + 128u * a + kk * 8,
+                                       smem_desc(va + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            ++c[a];
+                            if (j + 1 < it.nt[a]) {
+                                if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
+                                tc_fence_after();
+                                const int qs = (2 * n + a) % QSLOTS;
+                                issue_s(a, qs, (tv + 1) % KSTAGES);
+                                if (j + 2 == it.nt[a]) mma_commit(bar(B_QE + qs));  // the tile's last S
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit(bar(B_VE + tv % VSTAGES));
+                        if (j + 1 < it.nmax) mma_commit(bar(B_KE + (tv + 1) % KSTAGES));
+                    }
+                    if (ok) {
+                        for (int a = 0; a < QT; ++a)
+                            if (it.nt[a] > 0) mma_commit(bar(B_OF + a));
+                    }
+                    t += it.nmax;
                 }
-                if (ok) {
-                    for (int a = 0; a < QT; ++a)
-                        if (it.nt[a] > 0) mma_commit(bar(B_OF + a));
-                }
-                t += it.nmax;
             }
-            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-        }
-        if (lane == 0 && *abort_flag) {
-            // wait for the MMAs already issued before TMEM and shared memory are released
-            volatile int32_t dummy = 0;
-            mma_commit(bar(B_DRAIN));
-            mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
+            if (*abort_flag) {
+                // wait for the MMAs already issued before TMEM and shared memory are released
+                volatile int32_t dummy = 0;
+                mma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
+            }
         }
         __syncwarp();
     } else {
