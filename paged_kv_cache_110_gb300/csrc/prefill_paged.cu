@@ -468,6 +468,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // tensor cores work on the other.  One thread runs this role; the
         // warp's other lanes wait at the end.
         if (lane == 0) {
+            // shared-memory descriptors of the first Q, K and V buffers; a buffer or
+            // k-step further on adds its byte offset / 16 (the 14-bit address field
+            // cannot overflow below 256 KB)
+            const uint64_t desc_q = smem_desc(sb + OFF_Q, 16, 1024);
+            const uint64_t desc_k = smem_desc(sb + OFF_K, 16, 1024);
+            const uint64_t desc_v = smem_desc(sb + OFF_V, HALF_BYTES, 1024);
             int t = 0;               // K/V tiles consumed
             int c[QT] = {0, 0};      // S / P tiles per query tile
             bool ok = true;
@@ -486,12 +492,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                         return ok;
                     };
                     auto issue_s = [&](int a, int qs, int kst) {
-                        const uint32_t qa = sb + OFF_Q + qs * TILE_BYTES, ka = sb + OFF_K + kst * TILE_BYTES;
+                        const uint64_t qd = desc_q + uint64_t((qs * TILE_BYTES) >> 4);
+                        const uint64_t kd = desc_k + uint64_t((kst * TILE_BYTES) >> 4);
+                        const uint32_t dst = tmem + 128u * a;
     #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t hf = kk >> 2, ko = (kk & 3) * 32;
-                            mma_ss(tmem + 128u * a, smem_desc(qa + hf * HALF_BYTES + ko, 16, 1024),
-                                   smem_desc(ka + hf * HALF_BYTES + ko, 16, 1024), IDESC_QK, kk > 0);
+                            const uint64_t off = uint64_t(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+                            mma_ss(dst, qd + off, kd + off, IDESC_QK, kk > 0);
                         }
                         mma_commit(bar(B_SF + a));
                     };
@@ -520,11 +527,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                             if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
                             if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
                             tc_fence_after();
-                            const uint32_t va = sb + OFF_V + (tv % VSTAGES) * TILE_BYTES;
+                            const uint64_t vd = desc_v + uint64_t(((tv % VSTAGES) * TILE_BYTES) >> 4);
+                            const uint32_t dst = tmem + COL_O + 128u * a, src = tmem + 128u * a;
+                            const uint32_t acc0 = j > 0 ? 1u : 0u;
     #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(tmem + COL_O + 128u * a, tmem + 128u * a + kk * 8,
-                                       smem_desc(va + kk * 2048, HALF_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                                mma_ts(dst, src + kk * 8, vd + uint64_t((kk * 2048) >> 4), IDESC_PV, kk > 0 ? 1u : acc0);
                             ++c[a];
                             if (j + 1 < it.nt[a]) {
                                 if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
