@@ -77,6 +77,15 @@ def _load():
             lib.orc_prefill_weights.argtypes = pre + [i32, i32, i32, vp]
             lib.orc_decode.restype = i32
             lib.orc_decode.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, dbl, vp]
+            lib.orc_rmsnorm.restype = None
+            lib.orc_rmsnorm.argtypes = [vp, i32, vp, dbl, vp]
+            lib.orc_rope_cos_sin.restype = None
+            lib.orc_rope_cos_sin.argtypes = [dbl, i32, i64, vp]
+            lib.orc_rope_apply.restype = None
+            lib.orc_rope_apply.argtypes = [vp, i32, vp, vp]
+            lib.orc_norm_rope_store.restype = i32
+            lib.orc_norm_rope_store.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, dbl, vp, i64,
+                                                vp, vp, i64, i32, vp]
             _lib = lib
     return _lib
 
@@ -184,3 +193,56 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale):
                               bt.shape[1], _ptr(ctx), b, hq, hkv, d, float(scale), _ptr(out)),
            "orc_decode")
     return out
+
+
+def rmsnorm(x, weight=None, eps: float = 0.0) -> np.ndarray:
+    """x * 1/sqrt(mean(x^2) + eps) [* weight], in double (no rounding)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().orc_rmsnorm(_ptr(x), x.size, _ptr(w), float(eps), _ptr(y))
+    return y
+
+
+def rope_cos_sin(base: float, head_dim: int, max_positions: int) -> np.ndarray:
+    """[max_positions, head_dim] float32: cos(p * inv_freq) then sin(p * inv_freq)."""
+    t = np.empty((max_positions, head_dim), dtype=np.float32)
+    _load().orc_rope_cos_sin(float(base), head_dim, max_positions, _ptr(t))
+    return t
+
+
+def rope_apply(x, cos_sin_row) -> np.ndarray:
+    """Rotate one head vector (double) by one table row; pairs (i, i + d/2)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    cs = np.ascontiguousarray(cos_sin_row, dtype=np.float32)
+    y = np.empty_like(x)
+    _load().orc_rope_apply(_ptr(x), x.size, _ptr(cs), _ptr(y))
+    return y
+
+
+def norm_rope_store(qkv, num_heads, num_kv_heads, positions, cos_sin, q_weight, k_weight, eps,
+                    k_cache, v_cache, slot_mapping):
+    """Head RMSNorm + RoPE of Q and K and the KV write.  qkv: uint16 [T, (Hq + 2 Hkv) * d]
+    (any token stride); k_cache / v_cache uint16 [NB, bs, Hkv, d], written in place.
+    Returns q_out uint16 [T, Hq, d]."""
+    if qkv.dtype != np.uint16 or qkv.ndim != 2 or qkv.strides[1] != 2:
+        raise OracleError("qkv: expected uint16 [T, width] with packed rows")
+    d = cos_sin.shape[1]
+    t = qkv.shape[0]
+    if qkv.shape[1] != (num_heads + 2 * num_kv_heads) * d:
+        raise OracleError("qkv width does not match the head counts")
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or not c.flags.c_contiguous or c.ndim != 4 or c.shape[2:] != (num_kv_heads, d):
+            raise OracleError("caches: expected contiguous uint16 [NB, bs, Hkv, d]")
+    q_out = np.zeros((t, num_heads, d), dtype=np.uint16)
+    pos, sl = _i32(positions), _i32(slot_mapping)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    qw = None if q_weight is None else np.ascontiguousarray(q_weight, dtype=np.uint16)
+    kw = None if k_weight is None else np.ascontiguousarray(k_weight, dtype=np.uint16)
+    rc = _load().orc_norm_rope_store(_ptr(qkv), qkv.strides[0] // 2, t, num_heads, num_kv_heads, d, _ptr(pos),
+                                     _ptr(cs), cs.shape[0], _ptr(qw), _ptr(kw), float(eps), _ptr(q_out),
+                                     num_heads * d, _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                     k_cache.shape[1], _ptr(sl))
+    if rc not in (OK, BOUNDS):
+        raise OracleError(f"norm_rope_store: status {rc}")
+    return q_out, rc

@@ -15,7 +15,11 @@
  *        §19.1 softmax, §19.6 GQA.
  *   [P2] "大模型推理引擎入门：从 Continuous Batching 到 Scheduler，对着日志读懂
  *        nano-vllm" (juejin.cn), §2.7.2-2.7.3 prepare_prefill / prepare_decode.
- *   [P3] "VLLM on Fain的Blog" (Pico-vLLM log), #6 paged decode kernel.
+ *   [P3] "VLLM on Fain的Blog" (Pico-vLLM log), #6 paged decode kernel,
+ *        #8 fused RoPE and paged KV store.
+ *   [P4] "nano-vllm 技术分析" (deepseek.csdn.net), §4.3 RMSNorm, §4.4 RoPE.
+ *   [P1] also §12.2 (head norm and RoPE before the KV write), §19.5 RMSNorm,
+ *        §19.7 RoPE.
  *
  * What it computes is the plain definition of softmax attention, with K/V
  * rows fetched by walking block_table one key at a time.  There is no
@@ -300,6 +304,139 @@ int orc_decode(const uint16_t *q, int64_t q_stride,
         if (rc != ORC_OK) {
 #pragma omp critical
             status = rc;
+        }
+    }
+    return status;
+}
+
+
+/* ------------------------------------------------------------------ head norm, RoPE, KV write
+ *
+ * [P1] §12.2 and §19.7: after the fused QKV projection, every Q head and every
+ * K head (not V) is RMS-normalised over its own d features, then rotated by
+ * its token's position; the cache receives the rotated K and the plain V.
+ */
+
+/* Round a double to the nearest bf16 (ties to even), returned as its bits.
+ * Direct rounding to 8 significant bits, so no intermediate float rounding. */
+static uint16_t double_to_bf16(double x)
+{
+    float f;
+    uint32_t u;
+    if (isnan(x)) return 0x7fc0u;
+    if (x == 0.0 || isinf(x)) {
+        f = (float)x;
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    int e;
+    const double m = frexp(x, &e);            /* x = m * 2^e, 0.5 <= |m| < 1 */
+    double r = ldexp(nearbyint(ldexp(m, 8)), e - 8);  /* 8 significant bits, ties to even */
+    if (fabs(x) < 1.1754943508222875e-38)     /* below 2^-126: bf16's subnormal grid is 2^-133 */
+        r = ldexp(nearbyint(ldexp(x, 133)), -133);
+    if (fabs(r) > 3.3895313892515355e38) r = x > 0 ? INFINITY : -INFINITY;  /* past bf16's largest */
+    f = (float)r;                             /* exact: r has 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* [P1] §19.5; [P4] §4.3 RMSNorm.rms_forward: r = 1 / sqrt(mean(x^2) + eps),
+ * y = x * r, then (when w is given) y * w.  In double, no rounding. */
+void orc_rmsnorm(const double *x, int n, const double *w, double eps, double *y)
+{
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    const double r = 1.0 / sqrt(ss / n + eps);
+    for (int i = 0; i < n; ++i) y[i] = x[i] * r * (w ? w[i] : 1.0);
+}
+
+/* [P4] §4.4 RotaryEmbedding: inv_freq[i] = 1 / base^(2i / d) for i < d/2; the
+ * table row of position p is cos(p * inv_freq) followed by sin(p * inv_freq)
+ * (d values).  Computed in double and stored as float, the precision in
+ * which the table is held. */
+void orc_rope_cos_sin(double base, int d, int64_t max_positions, float *table)
+{
+    const int half = d / 2;
+    for (int64_t p = 0; p < max_positions; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double inv_freq = 1.0 / pow(base, (2.0 * i) / d);
+            const double phi = (double)p * inv_freq;
+            table[p * d + i] = (float)cos(phi);
+            table[p * d + half + i] = (float)sin(phi);
+        }
+}
+
+/* [P1] §19.7: feature i is paired with feature i + d/2 (the two halves, not
+ * neighbours); the pair (a, b) turns by phi: a' = a cos - b sin,
+ * b' = a sin + b cos.  cs is one table row (cos half, then sin half). */
+void orc_rope_apply(const double *x, int d, const float *cs, double *y)
+{
+    const int half = d / 2;
+    for (int i = 0; i < half; ++i) {
+        const double a = x[i], b = x[i + half];
+        const double c = cs[i], s = cs[half + i];
+        y[i] = a * c - b * s;
+        y[i + half] = a * s + b * c;
+    }
+}
+
+/* One head row, as the pages order it ([P1] §19.5 and §12.2): statistics and
+ * normalisation in float precision (here double), the result rounded to the
+ * activation dtype (bf16), multiplied by the bf16 weight and rounded again
+ * (w == NULL: no head norm); then RoPE on those values, rounded once to bf16. */
+static void norm_rope_row(const uint16_t *x_bits, int d, const uint16_t *w_bits, double eps, const float *cs,
+                          uint16_t *out_bits)
+{
+    double x[1024], y[1024];
+    for (int i = 0; i < d; ++i) x[i] = bf16_to_double(x_bits[i]);
+    if (w_bits) {
+        orc_rmsnorm(x, d, NULL, eps, y);
+        for (int i = 0; i < d; ++i) {
+            const double yn = bf16_to_double(double_to_bf16(y[i]));
+            x[i] = bf16_to_double(double_to_bf16(yn * bf16_to_double(w_bits[i])));
+        }
+    }
+    orc_rope_apply(x, d, cs, y);
+    for (int i = 0; i < d; ++i) out_bits[i] = double_to_bf16(y[i]);
+}
+
+/* [P3] #8 fused RoPE and paged KV store, with [P1] §12.2's head norm:
+ *   qkv       [T, (Hq + 2 Hkv) * d] bf16 bits, token stride qkv_stride; the
+ *             Q heads, then the K heads, then the V heads ([P4] qkv.split)
+ *   positions [T] int32, each in [0, max_positions)
+ *   cos_sin   [max_positions, d] float (orc_rope_cos_sin's layout)
+ *   q_weight, k_weight  [d] bf16 bits, or NULL for no head norm
+ *   q_out     [T, Hq, d] bf16 bits, token stride q_out_stride: rotated Q
+ *   k_cache, v_cache   pool rows `slot_mapping[t]` receive the rotated K and
+ *             the unchanged V; slot -1 skips the write (q_out is still written).
+ * A position outside the table or a slot outside the pool is reported
+ * (status 4) and that token is skipped. */
+int orc_norm_rope_store(const uint16_t *qkv, int64_t qkv_stride, int64_t num_tokens, int num_heads, int kv_heads,
+                        int d, const int32_t *positions, const float *cos_sin, int64_t max_positions,
+                        const uint16_t *q_weight, const uint16_t *k_weight, double eps,
+                        uint16_t *q_out, int64_t q_out_stride,
+                        uint16_t *k_cache, uint16_t *v_cache, int64_t num_blocks, int block_size,
+                        const int32_t *slot_mapping)
+{
+    if (d <= 0 || d > 1024 || d % 2 || num_heads <= 0 || kv_heads <= 0) return ORC_INVALID;
+    const int64_t row = (int64_t)kv_heads * d;
+    const int64_t num_slots = num_blocks * block_size;
+    int status = ORC_OK;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t p = positions[t], slot = slot_mapping[t];
+        if (p < 0 || p >= max_positions || (slot != -1 && (slot < 0 || slot >= num_slots))) {
+            status = ORC_BOUNDS;
+            continue;
+        }
+        const uint16_t *tok = qkv + t * qkv_stride;
+        const float *cs = cos_sin + p * d;
+        for (int h = 0; h < num_heads; ++h)
+            norm_rope_row(tok + (int64_t)h * d, d, q_weight, eps, cs, q_out + t * q_out_stride + (int64_t)h * d);
+        const int padding_row = slot == -1;  /* q is still rotated; nothing is stored */
+        for (int g = 0; g < kv_heads && !padding_row; ++g) {
+            norm_rope_row(tok + ((int64_t)num_heads + g) * d, d, k_weight, eps, cs, k_cache + slot * row + (int64_t)g * d);
+            for (int i = 0; i < d; ++i)
+                v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + kv_heads + g) * d + i];
         }
     }
     return status;

@@ -46,3 +46,11 @@ def brute_force_attention(q, k, v, scale, causal=True):
     w = np.exp(s)
     w /= w.sum(axis=-1, keepdims=True)
     return np.einsum("hij,jhd->ihd", w, vv), w
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round doubles to the nearest bf16 value (ties to even), still as doubles:
+    8 significant bits, without passing through float32."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)

@@ -27,6 +27,17 @@ MUTANTS = {
     "store_writes_k_to_v": ("v_cache[slot * row + e] = v[t * v_stride + e];",
                             "v_cache[slot * row + e] = k[t * k_stride + e];"),
     "store_drops_bounds_report": ("if (slot == -1) continue;", "if (slot < 0) continue;"),
+    "rmsnorm_sum_not_mean": ("sqrt(ss / n + eps)", "sqrt(ss + eps)"),
+    "rmsnorm_eps_outside_sqrt": ("sqrt(ss / n + eps)", "(sqrt(ss / n) + eps)"),
+    "rope_adjacent_pairs": ("const double a = x[i], b = x[i + half];",
+                            "const double a = x[(2 * i) % d], b = x[(2 * i + 1) % d];"),
+    "rope_sin_sign": ("y[i] = a * c - b * s;", "y[i] = a * c + b * s;"),
+    "rope_frequency_exponent": ("pow(base, (2.0 * i) / d)", "pow(base, (1.0 * i) / d)"),
+    "k_rotated_with_q_weight": ("d, k_weight, eps, cs, k_cache", "d, q_weight, eps, cs, k_cache"),
+    "v_cache_gets_k": ("v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + kv_heads + g) * d + i];",
+                       "v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + g) * d + i];"),
+    "rope_before_weight": ("x[i] = bf16_to_double(double_to_bf16(yn * bf16_to_double(w_bits[i])));",
+                           "x[i] = yn;"),
 }
 
 
@@ -42,6 +53,7 @@ def test_mutant_is_caught(name, tmp_path):
                    check=True, capture_output=True)
     env = dict(os.environ, PA_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_norm_rope.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
