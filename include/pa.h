@@ -91,6 +91,51 @@ pa_status pa_store_kvcache(const void *k, int64_t k_stride_tok, const void *v, i
                            const int32_t *slot_mapping, int32_t *dev_status, void *stream);
 
 /*
+ * Head RMSNorm, rotary position embedding and KV write in one pass
+ * ("大模型推理入门与 nano-vLLM 源码详解" §12.2, §19.3 RMSNorm, §19.7 RoPE;
+ * "nano-vllm 技术分析" §4.3-4.4; "VLLM on Fain的Blog" #8 fused RoPE and paged
+ * KV store).  For every token t:
+ *   - each Q head and each K head of qkv[t] is RMS-normalised over its
+ *     head_dim features (fp32 statistics, 1 / sqrt(mean(x^2) + eps), result
+ *     rounded to bf16, times the bf16 weight, rounded again), unless that
+ *     weight pointer is NULL;
+ *   - then rotated by position positions[t]: feature i pairs with feature
+ *     i + head_dim / 2 and (a, b) -> (a cos - b sin, a sin + b cos), with
+ *     cos / sin from row positions[t] of cos_sin (fp32 math, bf16 result);
+ *   - rotated Q goes to q_out[t]; rotated K and the unchanged V go to pool row
+ *     slot_mapping[t] of k_cache / v_cache.  slot -1 stores nothing (q_out[t]
+ *     is still written).
+ *
+ *   qkv           [num_tokens, (num_heads + 2 num_kv_heads) * head_dim] bf16,
+ *                 the Q heads, then the K heads, then the V heads of a token
+ *                 (the fused QKV projection's output); token stride
+ *                 qkv_stride_tok elements (a multiple of 8).
+ *   positions     [num_tokens] int32, each in [0, max_positions).
+ *   cos_sin       [max_positions, head_dim] fp32: cos(p * f_i) for the
+ *                 head_dim / 2 pairs, then sin(p * f_i), f_i = base^(-2i / head_dim)
+ *                 (the caller builds it once per model).
+ *   q_norm_weight, k_norm_weight   [head_dim] bf16 or NULL.
+ *   eps           added to mean(x^2), >= 0.
+ *   q_out         [num_tokens, num_heads, head_dim] bf16, token stride
+ *                 q_out_stride_tok (a multiple of 8).  It may be the Q part of
+ *                 qkv itself (same stride): each row is read before it is
+ *                 written.
+ *   k_cache, v_cache, num_blocks, block_size, slot_mapping   as for
+ *                 pa_store_kvcache.
+ * A position outside the table or a slot outside the pool sets PA_ERR_BOUNDS
+ * and that token is skipped.  Pointers must be 16-byte aligned.  The V copy
+ * is bit-exact; Q and K agree with an fp64 evaluation of the same steps up to
+ * the bf16 rounding of each step.
+ */
+pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_stride_tok, int64_t num_tokens,
+                                     int num_heads, int num_kv_heads, int head_dim,
+                                     const int32_t *positions, const float *cos_sin, int64_t max_positions,
+                                     const void *q_norm_weight, const void *k_norm_weight, float eps,
+                                     void *q_out, int64_t q_out_stride_tok,
+                                     void *k_cache, void *v_cache, int64_t num_blocks, int block_size,
+                                     const int32_t *slot_mapping, int32_t *dev_status, void *stream);
+
+/*
  * Causal varlen prefill ("大模型推理入门与 nano-vLLM 源码详解" §11.2, §13.2-13.3,
  * §10.2; flash_attn_varlen_func as nano-vLLM calls it, §20.5.2.2).
  * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and a key

@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
-    "pa_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+    "pa_store_kvcache", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
     "pa_decode_paged_noalloc",
 ]
 
@@ -44,6 +44,9 @@ def _load() -> ctypes.CDLL:
     L.pa_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
     L.pa_store_kvcache.restype = i32
     L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_norm_rope_store_kvcache.restype = i32
+    L.pa_norm_rope_store_kvcache.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, f32, vp, i64, vp, vp,
+                                             i64, i32, vp, vp, vp]
     L.pa_prefill_paged.restype = i32
     L.pa_prefill_paged.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32,
                                    i32, i32, i32, f32, vp, vp, vp]
@@ -128,6 +131,38 @@ def pa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stre
     _check(lib.pa_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], _ptr(k_cache),
                                 _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status), _stream(stream)),
            "pa_store_kvcache")
+
+
+def pa_norm_rope_store_kvcache(qkv, num_heads, num_kv_heads, positions, cos_sin, q_norm_weight, k_norm_weight,
+                               eps, q_out, k_cache, v_cache, slot_mapping, dev_status=None, stream=None):
+    """Head RMSNorm + RoPE of Q and K and the KV write.  qkv: CUDA bf16
+    [T, (Hq + 2 Hkv) * 128] (token stride free); positions / slot_mapping int32
+    [T]; cos_sin fp32 [max_positions, 128]; weights bf16 [128] or None;
+    q_out bf16 [T, Hq, 128] (may be a view of qkv's Q columns)."""
+    if qkv.dtype != torch.bfloat16 or qkv.dim() != 2 or not qkv.is_cuda or qkv.stride(1) != 1:
+        raise TypeError("qkv: expected a CUDA bf16 [T, width] tensor with packed rows")
+    nb, bs, hkv, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    if hkv != num_kv_heads or qkv.shape[1] != (num_heads + 2 * num_kv_heads) * d:
+        raise ValueError("qkv width or cache heads do not match the head counts")
+    hq, qs = _bf16_rows(q_out, "q_out")
+    if hq != num_heads or q_out.shape[0] != qkv.shape[0]:
+        raise ValueError("q_out must be [T, num_heads, head_dim]")
+    _i32(positions, "positions")
+    _i32(slot_mapping, "slot_mapping")
+    if positions.numel() != qkv.shape[0] or slot_mapping.numel() != qkv.shape[0]:
+        raise ValueError("positions and slot_mapping need one entry per token")
+    if cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or not cos_sin.is_contiguous() or cos_sin.shape[1] != d:
+        raise TypeError("cos_sin: expected a contiguous CUDA fp32 [max_positions, head_dim] tensor")
+    for w, name in ((q_norm_weight, "q_norm_weight"), (k_norm_weight, "k_norm_weight")):
+        if w is not None and (w.dtype != torch.bfloat16 or w.numel() != d or not w.is_contiguous()):
+            raise TypeError(f"{name}: expected a contiguous bf16 [head_dim] tensor or None")
+    _check(lib.pa_norm_rope_store_kvcache(_ptr(qkv), qkv.stride(0), qkv.shape[0], num_heads, num_kv_heads, d,
+                                          _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], _ptr(q_norm_weight),
+                                          _ptr(k_norm_weight), float(eps), _ptr(q_out), qs, _ptr(k_cache),
+                                          _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status),
+                                          _stream(stream)),
+           "pa_norm_rope_store_kvcache")
 
 
 def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, out, *, k=None, v=None,

@@ -1,0 +1,212 @@
+// rope_store.cu -- per-head RMSNorm of Q and K, rotary position embedding of
+// Q and K, and the KV write, in one pass over the fused QKV projection output.
+//
+// What it computes ("大模型推理入门与 nano-vLLM 源码详解" §12.2, §19.3, §19.7;
+// "nano-vllm 技术分析" §4.3-4.4; "VLLM on Fain的Blog" #8 fused RoPE and paged
+// KV store):
+//   - each Q head and each K head (not V) of a token is RMS-normalised over its
+//     128 features: statistics and scaling in fp32, the result rounded to bf16
+//     and multiplied by the bf16 weight (rounded again); without a weight this
+//     step is skipped;
+//   - the normalised vector is rotated by the token's position: feature i is
+//     paired with feature i + 64, and the pair (a, b) turns by the table's
+//     angle: a' = a cos - b sin, b' = a sin + b cos (fp32, rounded to bf16);
+//   - rotated Q goes to q_out; rotated K and the unchanged V go to pool row
+//     slot_mapping[t] (slot -1: nothing is stored).
+//
+// Design: bound by HBM (per token at Hq = 16, Hkv = 8: 8 KiB of QKV read, 4 KiB
+// of Q and 4 KiB of K/V written, 512 B of table read through L1/L2).  A
+// half-warp owns one 256-byte head row (16 lanes x 8 features, one 16-byte
+// load and store each); the sum of squares is reduced over the half-warp, and
+// the RoPE partner of lane l's features is lane l ^ 8.  Rows are numbered
+// token-major, Q heads first, then K heads, then V heads, so consecutive
+// half-warps read consecutive 256-byte pieces of the fused row.
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int D = pa::kHeadDim;
+constexpr int HALF = D / 2;
+constexpr unsigned FULL = 0xffffffffu;
+
+struct RopeParams {
+    const uint16_t *qkv;
+    int64_t qkv_stride;  // elements
+    int64_t num_tokens;
+    int num_heads, kv_heads;
+    const int32_t *positions;
+    const float *cos_sin;  // [max_positions, 128]: cos of the 64 pairs, then sin
+    int64_t max_positions;
+    const uint16_t *q_weight, *k_weight;  // [128] bf16 or null
+    float eps;
+    uint16_t *q_out;
+    int64_t q_out_stride;
+    uint16_t *k_cache, *v_cache;
+    int64_t num_slots;
+    const int32_t *slots;
+    int32_t *status;
+};
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = pa::bf16_lo(w[i]);
+        x[2 * i + 1] = pa::bf16_hi(w[i]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8])
+{
+    return make_uint4(pa::pack_bf16x2(x[0], x[1]), pa::pack_bf16x2(x[2], x[3]), pa::pack_bf16x2(x[4], x[5]),
+                      pa::pack_bf16x2(x[6], x[7]));
+}
+
+// Norm (when w != null) and rotate the 8 features of this lane; `sub` is the
+// lane's index within its half-warp, `cs` the token's table row.
+__device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint16_t *w, float eps, const float *cs, int sub)
+{
+    float x[8];
+    unpack8(raw, x);
+    // every lane of the warp runs the shuffles (the two half-warps may hold
+    // different kinds of row); offsets below 16 stay within a half-warp
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    if (w != nullptr) {
+        const float r = 1.0f / sqrtf(ss * (1.0f / D) + eps);
+        float wv[8];
+        unpack8(*reinterpret_cast<const uint4 *>(w + sub * 8), wv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = bf16_round(bf16_round(x[i] * r) * wv[i]);
+    }
+    // partner features (i +- 64) live in lane sub ^ 8
+    const uint4 mine = pack8(x);  // exact: x already holds bf16 values
+    uint4 other;
+    other.x = __shfl_xor_sync(FULL, mine.x, 8);
+    other.y = __shfl_xor_sync(FULL, mine.y, 8);
+    other.z = __shfl_xor_sync(FULL, mine.z, 8);
+    other.w = __shfl_xor_sync(FULL, mine.w, 8);
+    float y[8];
+    unpack8(other, y);
+    const int pair0 = (sub & 7) * 8;  // pair index of this lane's first feature
+    const float4 c0 = *reinterpret_cast<const float4 *>(cs + pair0);
+    const float4 c1 = *reinterpret_cast<const float4 *>(cs + pair0 + 4);
+    const float4 s0 = *reinterpret_cast<const float4 *>(cs + HALF + pair0);
+    const float4 s1 = *reinterpret_cast<const float4 *>(cs + HALF + pair0 + 4);
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float out[8];
+    if (sub < 8) {  // first half: a' = a cos - b sin, with b the partner
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = fmaf(x[i], c[i], -y[i] * s[i]);
+    } else {        // second half: b' = a sin + b cos, with a the partner
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = fmaf(y[i], s[i], x[i] * c[i]);
+    }
+    return pack8(out);
+}
+
+// One half-warp per head row; rows token-major (Q heads, K heads, V heads).
+__global__ void __launch_bounds__(256) norm_rope_store_kernel(const RopeParams p)
+{
+    const int sub = threadIdx.x & 15;
+    const int rows_per_token = p.num_heads + 2 * p.kv_heads;
+    const int64_t total = p.num_tokens * rows_per_token;
+    const int64_t step = int64_t(gridDim.x) * (blockDim.x >> 4);
+    // every lane of a warp runs the same number of iterations (the shuffles
+    // need both half-warps); a half-warp past the end works on nothing
+    const int64_t first = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+    const int64_t warp_first = first & ~int64_t(1);
+    for (int64_t base = warp_first; base < total; base += step) {
+        const int64_t row = base + ((threadIdx.x >> 4) & 1);
+        const bool live = row < total;
+        const int64_t t = live ? row / rows_per_token : 0;
+        const int r = live ? int(row - t * rows_per_token) : 0;
+        const int64_t pos = live ? p.positions[t] : 0;
+        const int64_t slot = live ? p.slots[t] : -1;
+        const bool bad = live && (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots)));
+        if (bad && sub == 0 && r == 0) pa::report(p.status, PA_ERR_BOUNDS);
+        const bool go = live && !bad;
+        const uint16_t *src = p.qkv + t * p.qkv_stride + int64_t(r) * D + sub * 8;
+        const uint4 raw = go ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
+        const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
+        const float *cs = p.cos_sin + (go ? pos : 0) * D;
+        // Q and K rows run the norm and rotation (with shuffles across the
+        // half-warp); the two half-warps of a warp may take different kinds of row
+        const bool rot = go && (is_q || is_k);
+        const uint16_t *w = is_q ? p.q_weight : p.k_weight;
+        // both half-warps must execute the shuffles: rows that do not rotate
+        // take part with zeros and discard the result
+        const uint4 y = norm_rope8(raw, rot ? w : nullptr, p.eps, rot ? cs : p.cos_sin, sub);
+        if (!go) continue;
+        if (is_q) {
+            *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
+        } else if (slot != -1) {
+            const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
+            uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (slot * p.kv_heads + g) * D + sub * 8;
+            *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw;
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_stride_tok, int64_t num_tokens,
+                                                int num_heads, int num_kv_heads, int head_dim,
+                                                const int32_t *positions, const float *cos_sin,
+                                                int64_t max_positions, const void *q_norm_weight,
+                                                const void *k_norm_weight, float eps, void *q_out,
+                                                int64_t q_out_stride_tok, void *k_cache, void *v_cache,
+                                                int64_t num_blocks, int block_size, const int32_t *slot_mapping,
+                                                int32_t *dev_status, void *stream)
+{
+    if (num_tokens < 0 || num_blocks < 0 || max_positions < 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != D || !pa::pow2_in(num_kv_heads, 1, 8) || num_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        !pa::pow2_in(num_heads / num_kv_heads, 1, 8))
+        return PA_ERR_UNSUPPORTED;
+    if (block_size < 16 || block_size > 1024 || block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!qkv || !positions || !cos_sin || !q_out || !k_cache || !v_cache || !slot_mapping || max_positions < 1)
+        return PA_ERR_INVALID_ARG;
+    if (qkv_stride_tok < int64_t(num_heads + 2 * num_kv_heads) * D || qkv_stride_tok % 8 != 0 ||
+        q_out_stride_tok < int64_t(num_heads) * D || q_out_stride_tok % 8 != 0)
+        return PA_ERR_INVALID_ARG;
+    for (const void *ptr : {qkv, static_cast<const void *>(cos_sin), static_cast<const void *>(q_out),
+                            static_cast<const void *>(k_cache), static_cast<const void *>(v_cache), q_norm_weight,
+                            k_norm_weight})
+        if (ptr != nullptr && !pa::aligned(ptr, 16)) return PA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return PA_ERR_INVALID_ARG;
+
+    RopeParams p;
+    p.qkv = static_cast<const uint16_t *>(qkv);
+    p.qkv_stride = qkv_stride_tok;
+    p.num_tokens = num_tokens;
+    p.num_heads = num_heads;
+    p.kv_heads = num_kv_heads;
+    p.positions = positions;
+    p.cos_sin = cos_sin;
+    p.max_positions = max_positions;
+    p.q_weight = static_cast<const uint16_t *>(q_norm_weight);
+    p.k_weight = static_cast<const uint16_t *>(k_norm_weight);
+    p.eps = eps;
+    p.q_out = static_cast<uint16_t *>(q_out);
+    p.q_out_stride = q_out_stride_tok;
+    p.k_cache = static_cast<uint16_t *>(k_cache);
+    p.v_cache = static_cast<uint16_t *>(v_cache);
+    p.num_slots = num_blocks * block_size;
+    p.slots = slot_mapping;
+    p.status = dev_status;
+    const int64_t rows = num_tokens * (num_heads + 2 * num_kv_heads);
+    const int64_t blocks = (rows + 15) / 16;  // 16 rows per 256-thread block
+    const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
+    const int64_t cap = int64_t(sms) * 8;
+    const unsigned grid = unsigned(blocks < cap ? blocks : cap);
+    norm_rope_store_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return pa::launch_status();
+}

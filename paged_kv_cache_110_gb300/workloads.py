@@ -198,6 +198,13 @@ class PagedBatch:
         return self.layout.block_tables
 
     @property
+    def positions(self) -> np.ndarray:
+        """int32 [T]: the position of every new token within its sequence (the
+        last query_lens[b] of context_lens[b] positions)."""
+        parts = [np.arange(c - n, c) for c, n in zip(self.context_lens, self.query_lens)]
+        return np.concatenate(parts).astype(np.int32) if parts else np.zeros(0, np.int32)
+
+    @property
     def num_tokens(self) -> int:
         return int(self.query_lens.sum())
 
@@ -302,3 +309,18 @@ def long_decode(device="cpu", num_seqs=512, seed=SEED_BASE + 5) -> PagedBatch:
     (about 8.6 GB of K+V per layer)."""
     ctx = rng(seed + 7).integers(1024, 4096, size=num_seqs, endpoint=True)
     return paged_batch(seed, ctx, np.ones_like(ctx), 256, num_blocks=8192, device=device)
+
+
+# ----------------------------------------------------------------- head norm and RoPE inputs
+
+ROPE_BASE = 1_000_000.0   # Qwen3's rope_theta
+RMS_EPS = 1e-6            # Qwen3-0.6B's rms_norm_eps (a configuration value; the pages name the field only)
+MAX_POSITIONS = 40_960    # Qwen3-0.6B's max_position_embeddings
+
+
+def norm_weights(seed: int, head_dim=HEAD_DIM, device="cpu"):
+    """(q_norm_weight, k_norm_weight): bf16 [head_dim] each, U[0.5, 1.5] (random
+    initialisation in the range of trained norm weights; no checkpoint)."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    w = (torch.rand((2, head_dim), generator=gen, dtype=torch.float32) + 0.5).to(torch.bfloat16)
+    return w[0].contiguous().to(device), w[1].contiguous().to(device)

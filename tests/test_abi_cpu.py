@@ -114,3 +114,25 @@ def test_decode_host_checks(lib):
     assert call(ns=-1) == 1
     assert call(ctx=None) == 1
     assert call(q=FAKE + 2) == 1   # q must be 16-byte aligned
+
+
+def test_norm_rope_store_host_checks(lib):
+    f = lib.pa_norm_rope_store_kvcache
+
+    def call(qkv=FAKE, qs=4096, nt=4, hq=16, hkv=8, d=128, pos=FAKE, cs=FAKE, mp=64, qw=None, kw=None, eps=1e-6,
+             qo=FAKE, qos=2048, kc=FAKE, vc=FAKE, nb=4, bs=16, sl=FAKE):
+        return f(qkv, qs, nt, hq, hkv, d, pos, cs, mp, qw, kw, ctypes.c_float(eps), qo, qos, kc, vc, nb, bs, sl,
+                 None, None)
+
+    assert call(d=64) == 2
+    assert call(hq=12) == 2
+    assert call(bs=8) == 2
+    assert call(nt=0) == 0
+    assert call(nt=-1) == 1
+    assert call(pos=None) == 1
+    assert call(cs=None) == 1
+    assert call(mp=0) == 1
+    assert call(qs=4000) == 1          # shorter than a fused row
+    assert call(qos=1024) == 1         # shorter than the Q heads
+    assert call(eps=-1.0) == 1
+    assert call(qw=FAKE + 8) == 1      # weight not 16-byte aligned
