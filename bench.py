@@ -386,6 +386,51 @@ def time_long_decode(device, steps, warmup, flush):
     return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512}
 
 
+def rope_store_bytes(num_tokens, hq=HQ, hkv=HKV):
+    """Algorithmic bytes of the fused head norm + RoPE + KV write per call: the
+    fused QKV row read, Q written, K and V rows written, position and slot read
+    (the cos/sin table and the norm weights are shared by all tokens and not
+    counted)."""
+    row = (hq + 2 * hkv) * D * 2
+    return num_tokens * (row + hq * D * 2 + 2 * hkv * D * 2 + 8)
+
+
+def time_rope_store(device, steps, warmup, flush):
+    """The fused head norm + RoPE + KV write on the varlen-prefill batch
+    (16,384-token budget, block size 256) and on the 256-token decode batch,
+    L2 flushed before each call."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    cs = pa.pa_rope_cos_sin_table(wl.ROPE_BASE, D, 4096, device=device)
+    qw, kw = wl.norm_weights(wl.SEED_BASE + 7, device=device)
+    res = {}
+    cases = {"varlen_16k": wl.varlen_prefill(device=device), "decode_256": wl.decode_batch(device=device)}
+    for name, b in cases.items():
+        q_out = torch.empty((b.num_tokens, HQ, D), dtype=torch.bfloat16, device=device)
+        pos = torch.as_tensor(b.positions, device=device)
+        sl = torch.as_tensor(b.slot_mapping, device=device)
+
+        def run():
+            pa.pa_norm_rope_store_kvcache(b.tokens.qkv, HQ, HKV, pos, cs, qw, kw, wl.RMS_EPS, q_out, b.k_cache,
+                                          b.v_cache, sl)
+
+        for _ in range(warmup):
+            run()
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            run()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) / 1e3)
+        t = statistics.median(times)
+        nbytes = rope_store_bytes(b.num_tokens)
+        res[name] = {"gbs": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "tokens": b.num_tokens}
+        del b
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle baseline
 
 
@@ -467,7 +512,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
-    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode"],
+    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode", "rope_store"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
     args = ap.parse_args()
@@ -487,6 +532,10 @@ def main():
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
         if args.leg == "prefill":
             res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
+        elif args.leg == "rope_store":
+            res = time_rope_store(device, max(args.steps, 1), args.warmup, flush)
+            for v in res.values():
+                v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         else:
             res = time_long_decode(device, max(args.steps, 1), args.warmup, flush)
         if rank == 0:
@@ -558,6 +607,11 @@ def main():
         ld = time_long_decode(device, max(args.steps, 5), 3, flush)
         ld["frac"] = ld["gbs"] / peaks["hbm_gbs"]
         line["long_decode"] = ld
+        torch.cuda.empty_cache()
+        rs = time_rope_store(device, max(args.steps, 5), 3, flush)
+        for v in rs.values():
+            v["frac"] = v["gbs"] / peaks["hbm_gbs"]
+        line["norm_rope_store"] = rs
         import oracle
         oracle.build()
         line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)

@@ -127,6 +127,16 @@ pa_status pa_store_kvcache(const void *k, int64_t k_stride_tok, const void *v, i
  * is bit-exact; Q and K agree with an fp64 evaluation of the same steps up to
  * the bf16 rounding of each step.
  */
+/*
+ * Fill the rotary table pa_norm_rope_store_kvcache reads ("nano-vllm 技术分析"
+ * §4.4 RotaryEmbedding; "大模型推理入门与 nano-vLLM 源码详解" §19.7, rope_theta):
+ * row p of table [max_positions, head_dim] fp32 (device) holds cos(p * f_i)
+ * for i < head_dim / 2, then sin(p * f_i), with f_i = base^(-2i / head_dim),
+ * evaluated in double precision and rounded to float.  base > 1, head_dim even
+ * and at most 1024; max_positions == 0 launches nothing.
+ */
+pa_status pa_rope_cos_sin_table(double base, int head_dim, int64_t max_positions, float *table, void *stream);
+
 pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_stride_tok, int64_t num_tokens,
                                      int num_heads, int num_kv_heads, int head_dim,
                                      const int32_t *positions, const float *cos_sin, int64_t max_positions,

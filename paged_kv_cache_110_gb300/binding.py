@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
-    "pa_store_kvcache", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+    "pa_store_kvcache", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
     "pa_decode_paged_noalloc",
 ]
 
@@ -44,6 +44,8 @@ def _load() -> ctypes.CDLL:
     L.pa_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
     L.pa_store_kvcache.restype = i32
     L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_rope_cos_sin_table.restype = i32
+    L.pa_rope_cos_sin_table.argtypes = [ctypes.c_double, i32, i64, vp, vp]
     L.pa_norm_rope_store_kvcache.restype = i32
     L.pa_norm_rope_store_kvcache.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, f32, vp, i64, vp, vp,
                                              i64, i32, vp, vp, vp]
@@ -131,6 +133,15 @@ def pa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stre
     _check(lib.pa_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], _ptr(k_cache),
                                 _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status), _stream(stream)),
            "pa_store_kvcache")
+
+
+def pa_rope_cos_sin_table(base: float, head_dim: int, max_positions: int, device=None, stream=None) -> torch.Tensor:
+    """fp32 [max_positions, head_dim] rotary table on the device (cos half, then sin half)."""
+    t = torch.empty((max_positions, head_dim), dtype=torch.float32,
+                    device=device if device is not None else torch.device("cuda"))
+    _check(lib.pa_rope_cos_sin_table(float(base), head_dim, max_positions, _ptr(t), _stream(stream)),
+           "pa_rope_cos_sin_table")
+    return t
 
 
 def pa_norm_rope_store_kvcache(qkv, num_heads, num_kv_heads, positions, cos_sin, q_norm_weight, k_norm_weight,

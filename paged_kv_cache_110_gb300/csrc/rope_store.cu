@@ -15,12 +15,13 @@
 //     slot_mapping[t] (slot -1: nothing is stored).
 //
 // Design: bound by HBM (per token at Hq = 16, Hkv = 8: 8 KiB of QKV read, 4 KiB
-// of Q and 4 KiB of K/V written, 512 B of table read through L1/L2).  A
-// half-warp owns one 256-byte head row (16 lanes x 8 features, one 16-byte
-// load and store each); the sum of squares is reduced over the half-warp, and
-// the RoPE partner of lane l's features is lane l ^ 8.  Rows are numbered
-// token-major, Q heads first, then K heads, then V heads, so consecutive
-// half-warps read consecutive 256-byte pieces of the fused row.
+// of Q and 4 KiB of K/V written, 512 B of table read through L1/L2).  A warp
+// owns 16 head rows of a token: it reads the token's position, slot and
+// table row, then the rows two at a time, a half-warp per 256-byte row (16
+// lanes x 8 features, one 16-byte load and store each), eight rows per
+// half-warp loaded before any is used so that many loads are in flight.  The sum of squares is
+// reduced over the half-warp, and the RoPE partner of lane l's features is
+// lane l ^ 8.
 #include "pa_common.cuh"
 
 namespace {
@@ -66,13 +67,14 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8])
 }
 
 // Norm (when w != null) and rotate the 8 features of this lane; `sub` is the
-// lane's index within its half-warp, `cs` the token's table row.
-__device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint16_t *w, float eps, const float *cs, int sub)
+// lane's index within its half-warp, c / s the cos and sin of the lane's 8
+// pairs.  Every lane of the warp must call this (it shuffles).
+__device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint4 *w, float eps, const float (&c)[8],
+                                            const float (&s)[8], int sub)
 {
     float x[8];
     unpack8(raw, x);
-    // every lane of the warp runs the shuffles (the two half-warps may hold
-    // different kinds of row); offsets below 16 stay within a half-warp
+    // offsets below 16 stay within a half-warp
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
@@ -81,7 +83,7 @@ __device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint16_t *w, float 
     if (w != nullptr) {
         const float r = 1.0f / sqrtf(ss * (1.0f / D) + eps);
         float wv[8];
-        unpack8(*reinterpret_cast<const uint4 *>(w + sub * 8), wv);
+        unpack8(*w, wv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = bf16_round(bf16_round(x[i] * r) * wv[i]);
     }
@@ -94,13 +96,6 @@ __device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint16_t *w, float 
     other.w = __shfl_xor_sync(FULL, mine.w, 8);
     float y[8];
     unpack8(other, y);
-    const int pair0 = (sub & 7) * 8;  // pair index of this lane's first feature
-    const float4 c0 = *reinterpret_cast<const float4 *>(cs + pair0);
-    const float4 c1 = *reinterpret_cast<const float4 *>(cs + pair0 + 4);
-    const float4 s0 = *reinterpret_cast<const float4 *>(cs + HALF + pair0);
-    const float4 s1 = *reinterpret_cast<const float4 *>(cs + HALF + pair0 + 4);
-    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
     float out[8];
     if (sub < 8) {  // first half: a' = a cos - b sin, with b the partner
 #pragma unroll
@@ -112,50 +107,99 @@ __device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint16_t *w, float 
     return pack8(out);
 }
 
-// One half-warp per head row; rows token-major (Q heads, K heads, V heads).
-__global__ void __launch_bounds__(256) norm_rope_store_kernel(const RopeParams p)
+constexpr int CHUNK = 8;  // rows per half-warp whose loads are issued together
+
+// Work unit: 2 * CHUNK consecutive head rows (Q heads, K heads, V heads) of
+// one token, a warp per unit (grid-stride).  The token's position, slot and
+// table row are read per unit (the second unit of a token finds them in L1);
+// the half-warps take alternate rows, CHUNK rows each, all loaded before any
+// is used.
+__global__ void __launch_bounds__(128) norm_rope_store_kernel(const RopeParams p)
 {
-    const int sub = threadIdx.x & 15;
-    const int rows_per_token = p.num_heads + 2 * p.kv_heads;
-    const int64_t total = p.num_tokens * rows_per_token;
-    const int64_t step = int64_t(gridDim.x) * (blockDim.x >> 4);
-    // every lane of a warp runs the same number of iterations (the shuffles
-    // need both half-warps); a half-warp past the end works on nothing
-    const int64_t first = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-    const int64_t warp_first = first & ~int64_t(1);
-    for (int64_t base = warp_first; base < total; base += step) {
-        const int64_t row = base + ((threadIdx.x >> 4) & 1);
-        const bool live = row < total;
-        const int64_t t = live ? row / rows_per_token : 0;
-        const int r = live ? int(row - t * rows_per_token) : 0;
-        const int64_t pos = live ? p.positions[t] : 0;
-        const int64_t slot = live ? p.slots[t] : -1;
-        const bool bad = live && (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots)));
-        if (bad && sub == 0 && r == 0) pa::report(p.status, PA_ERR_BOUNDS);
-        const bool go = live && !bad;
-        const uint16_t *src = p.qkv + t * p.qkv_stride + int64_t(r) * D + sub * 8;
-        const uint4 raw = go ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
-        const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
-        const float *cs = p.cos_sin + (go ? pos : 0) * D;
-        // Q and K rows run the norm and rotation (with shuffles across the
-        // half-warp); the two half-warps of a warp may take different kinds of row
-        const bool rot = go && (is_q || is_k);
-        const uint16_t *w = is_q ? p.q_weight : p.k_weight;
-        // both half-warps must execute the shuffles: rows that do not rotate
-        // take part with zeros and discard the result
-        const uint4 y = norm_rope8(raw, rot ? w : nullptr, p.eps, rot ? cs : p.cos_sin, sub);
-        if (!go) continue;
-        if (is_q) {
-            *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
-        } else if (slot != -1) {
-            const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
-            uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (slot * p.kv_heads + g) * D + sub * 8;
-            *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw;
+    const int lane = threadIdx.x & 31, sub = lane & 15, hw = lane >> 4;
+    const int rows = p.num_heads + 2 * p.kv_heads;
+    const int units_per_token = (rows + 2 * CHUNK - 1) / (2 * CHUNK);
+    const int64_t units = p.num_tokens * units_per_token;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    uint4 wq = make_uint4(0, 0, 0, 0), wk = wq;
+    if (p.q_weight) wq = *reinterpret_cast<const uint4 *>(p.q_weight + sub * 8);
+    if (p.k_weight) wk = *reinterpret_cast<const uint4 *>(p.k_weight + sub * 8);
+    for (int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < units; u += warps) {
+        const int64_t t = u / units_per_token;
+        const int r0 = int(u - t * units_per_token) * 2 * CHUNK;
+        const int64_t pos = p.positions[t], slot = p.slots[t];
+        if (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots))) {
+            if (lane == 0 && r0 == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            continue;  // the whole warp skips the unit
+        }
+        const uint16_t *src = p.qkv + t * p.qkv_stride + sub * 8;
+        uint4 raw[CHUNK];
+#pragma unroll
+        for (int k = 0; k < CHUNK; ++k) {
+            const int r = r0 + 2 * k + hw;
+            raw[k] = r < rows ? *reinterpret_cast<const uint4 *>(src + int64_t(r) * D) : make_uint4(0, 0, 0, 0);
+        }
+        const float *cs = p.cos_sin + pos * D + (sub & 7) * 8;
+        float c[8], s[8];
+        {
+            const float4 c0 = *reinterpret_cast<const float4 *>(cs), c1 = *reinterpret_cast<const float4 *>(cs + 4);
+            const float4 s0 = *reinterpret_cast<const float4 *>(cs + HALF);
+            const float4 s1 = *reinterpret_cast<const float4 *>(cs + HALF + 4);
+            c[0] = c0.x, c[1] = c0.y, c[2] = c0.z, c[3] = c0.w, c[4] = c1.x, c[5] = c1.y, c[6] = c1.z, c[7] = c1.w;
+            s[0] = s0.x, s[1] = s0.y, s[2] = s0.z, s[3] = s0.w, s[4] = s1.x, s[5] = s1.y, s[6] = s1.z, s[7] = s1.w;
+        }
+#pragma unroll
+        for (int k = 0; k < CHUNK; ++k) {
+            const int r = r0 + 2 * k + hw;
+            if (r0 + 2 * k >= rows) break;  // warp-uniform: no row left for either half-warp
+            const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
+            const bool has_w = is_q ? p.q_weight != nullptr : (is_k && p.k_weight != nullptr);
+            const uint4 y = norm_rope8(raw[k], has_w ? (is_q ? &wq : &wk) : nullptr, p.eps, c, s, sub);
+            if (r >= rows) continue;
+            if (is_q) {
+                *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
+            } else if (slot != -1) {
+                const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
+                uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (slot * p.kv_heads + g) * D + sub * 8;
+                *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw[k];
+            }
         }
     }
 }
 
+// Row p of the table: cos(p * f_i) for i < head_dim / 2, then sin(p * f_i),
+// f_i = base^(-2i / head_dim); double precision, stored as float.
+__global__ void __launch_bounds__(256) rope_table_kernel(double base, int head_dim, int64_t max_positions,
+                                                         float *table)
+{
+    const int half = head_dim / 2;
+    const int64_t total = max_positions * half;
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < total; k += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t p = k / half;
+        const int i = int(k - p * half);
+        const double inv_freq = 1.0 / pow(base, double(2 * i) / head_dim);
+        double sn, cn;
+        sincos(double(p) * inv_freq, &sn, &cn);
+        table[p * head_dim + i] = float(cn);
+        table[p * head_dim + half + i] = float(sn);
+    }
+}
+
 }  // namespace
+
+extern "C" pa_status pa_rope_cos_sin_table(double base, int head_dim, int64_t max_positions, float *table,
+                                           void *stream)
+{
+    if (!(base > 1.0) || head_dim <= 0 || head_dim % 2 != 0 || head_dim > 1024 || max_positions < 0)
+        return PA_ERR_INVALID_ARG;
+    if (max_positions == 0) return PA_OK;
+    if (table == nullptr) return PA_ERR_INVALID_ARG;
+    const int64_t total = max_positions * (head_dim / 2);
+    const int64_t blocks = (total + 255) / 256;
+    const unsigned grid = unsigned(blocks < 4096 ? blocks : 4096);
+    rope_table_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(base, head_dim, max_positions, table);
+    return pa::launch_status();
+}
 
 extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_stride_tok, int64_t num_tokens,
                                                 int num_heads, int num_kv_heads, int head_dim,
@@ -202,11 +246,12 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     p.num_slots = num_blocks * block_size;
     p.slots = slot_mapping;
     p.status = dev_status;
-    const int64_t rows = num_tokens * (num_heads + 2 * num_kv_heads);
-    const int64_t blocks = (rows + 15) / 16;  // 16 rows per 256-thread block
+    // a warp per unit of 16 head rows, four warps per block
+    const int64_t units = num_tokens * ((num_heads + 2 * num_kv_heads + 15) / 16);
+    const int64_t blocks = (units + 3) / 4;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
-    const int64_t cap = int64_t(sms) * 8;
+    const int64_t cap = int64_t(sms) * 16;
     const unsigned grid = unsigned(blocks < cap ? blocks : cap);
-    norm_rope_store_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    norm_rope_store_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return pa::launch_status();
 }

@@ -136,3 +136,12 @@ def test_norm_rope_store_host_checks(lib):
     assert call(qos=1024) == 1         # shorter than the Q heads
     assert call(eps=-1.0) == 1
     assert call(qw=FAKE + 8) == 1      # weight not 16-byte aligned
+
+
+def test_rope_table_host_checks(lib):
+    f = lib.pa_rope_cos_sin_table
+    assert f(1e6, 127, 16, FAKE, None) == 1   # odd head_dim
+    assert f(1.0, 128, 16, FAKE, None) == 1   # base must exceed 1
+    assert f(1e6, 128, -1, FAKE, None) == 1
+    assert f(1e6, 128, 0, FAKE, None) == 0    # nothing to fill
+    assert f(1e6, 128, 16, None, None) == 1

@@ -160,3 +160,14 @@ def test_host_errors_return_before_launch():
         pa().pa_norm_rope_store_kvcache(batch.tokens.qkv, 16, 8, i32(batch.positions, d), cs, None, None, -1.0,
                                         q_out, batch.k_cache, batch.v_cache, i32(batch.slot_mapping, d))
     assert e.value.status == pa().PA_ERR_INVALID_ARG
+
+
+def test_device_table_matches_oracle_table():
+    d = dev()
+    got = pa().pa_rope_cos_sin_table(wl.ROPE_BASE, 128, 4096, device=d).cpu().numpy()
+    ref = oracle.rope_cos_sin(wl.ROPE_BASE, 128, 4096)
+    # both evaluate in double and round once to float: equal up to one float unit
+    # where the two double evaluations straddle a float rounding boundary
+    diff = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    ulp = np.spacing(np.abs(ref)).astype(np.float64)
+    assert (diff <= ulp).all() and (got == ref).mean() > 0.999
