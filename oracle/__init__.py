@@ -83,6 +83,10 @@ def _load():
             lib.orc_rope_cos_sin.argtypes = [dbl, i32, i64, vp]
             lib.orc_rope_apply.restype = None
             lib.orc_rope_apply.argtypes = [vp, i32, vp, vp]
+            lib.orc_prepare_prefill.restype = i32
+            lib.orc_prepare_prefill.argtypes = [vp, vp, vp, i32, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp]
+            lib.orc_prepare_decode.restype = i32
+            lib.orc_prepare_decode.argtypes = [vp, i32, vp, i32, i32, i64, vp, vp, vp]
             lib.orc_norm_rope_store.restype = i32
             lib.orc_norm_rope_store.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, dbl, vp, i64,
                                                 vp, vp, i64, i32, vp]
@@ -246,3 +250,36 @@ def norm_rope_store(qkv, num_heads, num_kv_heads, positions, cos_sin, q_weight, 
     if rc not in (OK, BOUNDS):
         raise OracleError(f"norm_rope_store: status {rc}")
     return q_out, rc
+
+
+def _table2d(block_table, num_seqs):
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    if bt.ndim != 2 or bt.shape[0] != num_seqs:
+        raise OracleError("block_table must be [num_seqs, max_blocks]")
+    return bt
+
+
+def prepare_prefill(seq_lens, num_cached, num_scheduled, block_table, block_size, num_blocks):
+    """Step metadata of a prefill batch; returns a dict of int32 arrays / ints and the status."""
+    sl, nc, ns = _i32(seq_lens), _i32(num_cached), _i32(num_scheduled)
+    b = sl.size
+    bt = _table2d(block_table, b)
+    t = int(ns.sum())
+    cu_q, cu_k = np.zeros(b + 1, np.int32), np.zeros(b + 1, np.int32)
+    pos, slots = np.zeros(t, np.int32), np.zeros(t, np.int32)
+    mq, mk = ctypes.c_int32(), ctypes.c_int32()
+    rc = _load().orc_prepare_prefill(_ptr(sl), _ptr(nc), _ptr(ns), b, _ptr(bt), bt.shape[1], block_size, num_blocks,
+                                     _ptr(cu_q), _ptr(cu_k), _ptr(pos), _ptr(slots), ctypes.byref(mq),
+                                     ctypes.byref(mk))
+    return {"cu_seqlens_q": cu_q, "cu_seqlens_k": cu_k, "positions": pos, "slot_mapping": slots,
+            "max_seqlen_q": mq.value, "max_seqlen_k": mk.value}, rc
+
+
+def prepare_decode(seq_lens, block_table, block_size, num_blocks):
+    sl = _i32(seq_lens)
+    b = sl.size
+    bt = _table2d(block_table, b)
+    pos, ctx, slots = np.zeros(b, np.int32), np.zeros(b, np.int32), np.zeros(b, np.int32)
+    rc = _load().orc_prepare_decode(_ptr(sl), b, _ptr(bt), bt.shape[1], block_size, num_blocks, _ptr(pos), _ptr(ctx),
+                                    _ptr(slots))
+    return {"positions": pos, "context_lens": ctx, "slot_mapping": slots}, rc

@@ -17,7 +17,9 @@
  *        nano-vllm" (juejin.cn), §2.7.2-2.7.3 prepare_prefill / prepare_decode.
  *   [P3] "VLLM on Fain的Blog" (Pico-vLLM log), #6 paged decode kernel,
  *        #8 fused RoPE and paged KV store.
- *   [P4] "nano-vllm 技术分析" (deepseek.csdn.net), §4.3 RMSNorm, §4.4 RoPE.
+ *   [P4] "nano-vllm 技术分析" (deepseek.csdn.net), §4.3 RMSNorm, §4.4 RoPE,
+ *        the prefill parameter computation (prepare_prefill).
+ *   [P2] also §2.7.2-2.7.3 worked prepare_prefill / prepare_decode values.
  *   [P1] also §12.2 (head norm and RoPE before the KV write), §19.5 RMSNorm,
  *        §19.7 RoPE.
  *
@@ -437,6 +439,97 @@ int orc_norm_rope_store(const uint16_t *qkv, int64_t qkv_stride, int64_t num_tok
             norm_rope_row(tok + ((int64_t)num_heads + g) * d, d, k_weight, eps, cs, k_cache + slot * row + (int64_t)g * d);
             for (int i = 0; i < d; ++i)
                 v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + kv_heads + g) * d + i];
+        }
+    }
+    return status;
+}
+
+
+/* ------------------------------------------------------------------ step metadata
+ *
+ * [P4] prepare_prefill, step by step, for sequence b of the batch:
+ *   seqlen = seq_lens[b] (cached + uncached tokens); start = min(num_cached,
+ *   seqlen - 1) (a fully cached prompt still computes its last token);
+ *   seqlen_q = num_scheduled; end = start + seqlen_q; positions start..end-1;
+ *   cu_seqlens_q += seqlen_q; cu_seqlens_k += seqlen_k; slots block by block
+ *   from start_block = start / bs to end_block = ceil(end / bs), the first
+ *   block starting at start % bs and the last one ending at end.
+ * seqlen_k is taken as `end`: the page writes `seqlen`, which is the same
+ * whenever the rest of the prompt is scheduled at once; for a chunk, the keys
+ * its last query may read end at `end` ([P1] §8.2, §11.2's key lengths).
+ * A table entry that is not a block of the pool gives slot -1 and status 4;
+ * end > seqlen or seqlen_q < 1 gives status 1.
+ */
+int orc_prepare_prefill(const int32_t *seq_lens, const int32_t *num_cached, const int32_t *num_scheduled,
+                        int num_seqs, const int32_t *block_table, int max_blocks, int block_size, int64_t num_blocks,
+                        int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *positions, int32_t *slot_mapping,
+                        int32_t *max_seqlen_q, int32_t *max_seqlen_k)
+{
+    int status = ORC_OK;
+    int64_t nq = 0;
+    cu_seqlens_q[0] = 0;
+    cu_seqlens_k[0] = 0;
+    *max_seqlen_q = 0;
+    *max_seqlen_k = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int seqlen = seq_lens[b];
+        const int start = num_cached[b] < seqlen - 1 ? num_cached[b] : seqlen - 1;
+        const int seqlen_q = num_scheduled[b];
+        const int end = start + seqlen_q;
+        if (seqlen_q < 1 || start < 0 || end > seqlen) status = ORC_INVALID;
+        const int seqlen_k = end;
+        for (int p = start; p < end; ++p) positions[nq + p - start] = p;
+        cu_seqlens_q[b + 1] = cu_seqlens_q[b] + seqlen_q;
+        cu_seqlens_k[b + 1] = cu_seqlens_k[b] + seqlen_k;
+        if (seqlen_q > *max_seqlen_q) *max_seqlen_q = seqlen_q;
+        if (seqlen_k > *max_seqlen_k) *max_seqlen_k = seqlen_k;
+        const int32_t *table = block_table + (int64_t)b * max_blocks;
+        const int start_block = start / block_size;
+        const int end_block = (end + block_size - 1) / block_size;
+        int64_t k = nq;
+        for (int i = start_block; i < end_block; ++i) {
+            const int ok = i < max_blocks && table[i] >= 0 && table[i] < num_blocks;
+            if (!ok) status = ORC_BOUNDS;
+            const int64_t base = ok ? (int64_t)table[i] * block_size : 0;
+            int64_t slot_start = base, slot_end = base + block_size;
+            if (i == start_block) slot_start += start % block_size;
+            if (i == end_block - 1) slot_end = base + end - (int64_t)i * block_size;
+            for (int64_t sl = slot_start; sl < slot_end; ++sl) slot_mapping[k++] = ok ? (int32_t)sl : -1;
+        }
+        nq += seqlen_q;
+    }
+    return status;
+}
+
+/* [P2] §2.7.3 and [P1] §11.4 prepare_decode: every sequence adds its last
+ * token: position = seqlen - 1, context_lens = seqlen, slot = the table's
+ * last block used (block (seqlen - 1) / bs) * bs + last_block_num_tokens - 1.
+ * seqlen 0 is a padding row ([P1] §13.5): position 0, context 0, slot -1. */
+int orc_prepare_decode(const int32_t *seq_lens, int num_seqs, const int32_t *block_table, int max_blocks,
+                       int block_size, int64_t num_blocks, int32_t *positions, int32_t *context_lens,
+                       int32_t *slot_mapping)
+{
+    int status = ORC_OK;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int seqlen = seq_lens[b];
+        if (seqlen < 0) status = ORC_INVALID;
+        if (seqlen <= 0) {
+            positions[b] = 0;
+            context_lens[b] = 0;
+            slot_mapping[b] = -1;
+            continue;
+        }
+        const int num_blocks_seq = (seqlen + block_size - 1) / block_size;
+        const int last_block_num_tokens = seqlen - (num_blocks_seq - 1) * block_size;
+        positions[b] = seqlen - 1;
+        context_lens[b] = seqlen;
+        const int last = num_blocks_seq - 1;
+        const int32_t id = last < max_blocks ? block_table[(int64_t)b * max_blocks + last] : -1;
+        if (id < 0 || id >= num_blocks) {
+            status = ORC_BOUNDS;
+            slot_mapping[b] = -1;
+        } else {
+            slot_mapping[b] = (int32_t)((int64_t)id * block_size + last_block_num_tokens - 1);
         }
     }
     return status;

@@ -36,6 +36,15 @@ MUTANTS = {
     "k_rotated_with_q_weight": ("d, k_weight, eps, cs, k_cache", "d, q_weight, eps, cs, k_cache"),
     "v_cache_gets_k": ("v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + kv_heads + g) * d + i];",
                        "v_cache[slot * row + (int64_t)g * d + i] = tok[((int64_t)num_heads + g) * d + i];"),
+    "meta_start_ignores_cache": ("const int start = num_cached[b] < seqlen - 1 ? num_cached[b] : seqlen - 1;",
+                                 "const int start = 0;"),
+    "meta_keys_are_queries": ("const int seqlen_k = end;", "const int seqlen_k = seqlen_q;"),
+    "meta_first_block_offset_dropped": ("if (i == start_block) slot_start += start % block_size;",
+                                        "if (i == start_block) slot_start += 0;"),
+    "meta_last_block_full": ("if (i == end_block - 1) slot_end = base + end - (int64_t)i * block_size;",
+                             "if (i == end_block - 1) slot_end = base + block_size;"),
+    "meta_decode_position_is_length": ("positions[b] = seqlen - 1;", "positions[b] = seqlen;"),
+    "meta_decode_slot_first_block": ("block_table[(int64_t)b * max_blocks + last]", "block_table[(int64_t)b * max_blocks]"),
     "rope_before_weight": ("x[i] = bf16_to_double(double_to_bf16(yn * bf16_to_double(w_bits[i])));",
                            "x[i] = yn;"),
 }
@@ -54,6 +63,7 @@ def test_mutant_is_caught(name, tmp_path):
     env = dict(os.environ, PA_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_norm_rope.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_norm_rope.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_metadata.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
