@@ -431,6 +431,55 @@ def time_rope_store(device, steps, warmup, flush):
     return res
 
 
+def time_step_metadata(device, steps, warmup):
+    """Device-built step metadata: the varlen-prefill batch (counts and tables
+    of ~20 sequences, 16K tokens expanded) and a 512-sequence decode batch;
+    microseconds per call (launch-bound work: no L2 flush)."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    res = {}
+    v = wl.varlen_prefill(device="cpu")
+    lens = torch.as_tensor(v.context_lens, device=device)
+    zeros = torch.zeros_like(lens)
+    vt = torch.as_tensor(v.block_tables, device=device)
+    t_tokens = int(v.query_lens.sum())
+    rng = wl.rng(wl.SEED_BASE + 5)
+    dl = torch.as_tensor(rng.integers(1024, 4096, 512, endpoint=True).astype(np.int32), device=device)
+    dt = torch.as_tensor(rng.permutation(512 * 16).astype(np.int32).reshape(512, 16), device=device)
+    cases = {
+        "prefill_varlen_16k": (lambda: pa.pa_prepare_prefill(lens, zeros, lens, vt, 256, v.layout.num_blocks, t_tokens),
+                               {"seqs": int(lens.numel()), "tokens": t_tokens}),
+        "decode_512": (lambda: pa.pa_prepare_decode(dl, dt, 256, 512 * 16), {"seqs": 512}),
+    }
+    reps = 20
+    for name, (fn, info) in cases.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        # device time: the calls are captured in a CUDA graph (they are
+        # capturable by design) and replayed, so host overhead is excluded
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph):
+                for _ in range(reps):
+                    fn()
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(steps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            graph.replay()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) * 1e3 / reps)
+        res[name] = dict(info, us=statistics.median(times), timing="CUDA graph of %d calls, per call" % reps)
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle baseline
 
 
@@ -512,7 +561,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
-    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode", "rope_store"],
+    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode", "rope_store", "metadata"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
     args = ap.parse_args()
@@ -532,6 +581,8 @@ def main():
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
         if args.leg == "prefill":
             res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
+        elif args.leg == "metadata":
+            res = time_step_metadata(device, max(args.steps, 1), args.warmup)
         elif args.leg == "rope_store":
             res = time_rope_store(device, max(args.steps, 1), args.warmup, flush)
             for v in res.values():
@@ -612,6 +663,7 @@ def main():
         for v in rs.values():
             v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         line["norm_rope_store"] = rs
+        line["step_metadata"] = time_step_metadata(device, max(args.steps, 5), 3)
         import oracle
         oracle.build()
         line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)

@@ -146,6 +146,49 @@ pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_stride_tok, in
                                      const int32_t *slot_mapping, int32_t *dev_status, void *stream);
 
 /*
+ * Step metadata of a prefill batch, built on the device ("nano-vllm 技术分析",
+ * prepare_prefill; "大模型推理引擎入门 ... 对着日志读懂 nano-vllm" §2.7.2;
+ * "大模型推理入门与 nano-vLLM 源码详解" §11.2-11.3).  For sequence b with
+ * seq_lens[b] tokens of which num_cached[b] are in the cache, and
+ * num_scheduled[b] scheduled this step:
+ *   start = min(num_cached, seq_len - 1), end = start + num_scheduled;
+ *   positions of its tokens: start .. end-1 (concatenated in sequence order);
+ *   cu_seqlens_q: prefix sums of num_scheduled; cu_seqlens_k: of end (the
+ *   keys its last query reads: the whole prompt once the rest is scheduled);
+ *   max_seqlens[0] / [1]: the largest num_scheduled / end;
+ *   slot_mapping[token] = block_table[b][pos / block_size] * block_size +
+ *   pos % block_size.
+ *   seq_lens, num_cached, num_scheduled   [num_seqs] int32 (device)
+ *   block_table   [num_seqs, max_blocks] int32 (device)
+ *   cu_seqlens_q, cu_seqlens_k   [num_seqs + 1] int32 out
+ *   positions, slot_mapping      [max_tokens] int32 out (capacity)
+ *   max_seqlens   [2] int32 out
+ * A sequence with num_scheduled < 1 or end > seq_len sets PA_ERR_INVALID_ARG
+ * and contributes no tokens; a table entry outside the pool gives slot -1 and
+ * PA_ERR_BOUNDS; tokens past max_tokens set PA_ERR_BOUNDS and are not written.
+ * Two launches on `stream`; graph-capturable.
+ */
+pa_status pa_prepare_prefill(const int32_t *seq_lens, const int32_t *num_cached, const int32_t *num_scheduled,
+                             int num_seqs, const int32_t *block_table, int max_blocks, int block_size,
+                             int64_t num_blocks, int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *positions,
+                             int32_t *slot_mapping, int64_t max_tokens, int32_t *max_seqlens, int32_t *dev_status,
+                             void *stream);
+
+/*
+ * Step metadata of a decode batch, built on the device
+ * ("大模型推理引擎入门 ... 对着日志读懂 nano-vllm" §2.7.3; "大模型推理入门与
+ * nano-vLLM 源码详解" §11.4, §13.5): sequence b adds its last token:
+ * positions[b] = seq_lens[b] - 1, context_lens[b] = seq_lens[b], slot_mapping[b]
+ * = the slot of that position.  seq_lens[b] == 0 marks a padding row (a CUDA
+ * graph's spare batch entry): position 0, context 0, slot -1.  All arrays are
+ * [num_seqs] int32 on the device.  A table entry outside the pool gives slot
+ * -1 and PA_ERR_BOUNDS; a negative length sets PA_ERR_INVALID_ARG.
+ */
+pa_status pa_prepare_decode(const int32_t *seq_lens, int num_seqs, const int32_t *block_table, int max_blocks,
+                            int block_size, int64_t num_blocks, int32_t *positions, int32_t *context_lens,
+                            int32_t *slot_mapping, int32_t *dev_status, void *stream);
+
+/*
  * Causal varlen prefill ("大模型推理入门与 nano-vLLM 源码详解" §11.2, §13.2-13.3,
  * §10.2; flash_attn_varlen_func as nano-vLLM calls it, §20.5.2.2).
  * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and a key

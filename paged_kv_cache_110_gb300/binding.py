@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
-    "pa_store_kvcache", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+    "pa_store_kvcache", "pa_prepare_prefill", "pa_prepare_decode", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
     "pa_decode_paged_noalloc",
 ]
 
@@ -44,6 +44,10 @@ def _load() -> ctypes.CDLL:
     L.pa_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
     L.pa_store_kvcache.restype = i32
     L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_prepare_prefill.restype = i32
+    L.pa_prepare_prefill.argtypes = [vp, vp, vp, i32, vp, i32, i32, i64, vp, vp, vp, vp, i64, vp, vp, vp]
+    L.pa_prepare_decode.restype = i32
+    L.pa_prepare_decode.argtypes = [vp, i32, vp, i32, i32, i64, vp, vp, vp, vp, vp]
     L.pa_rope_cos_sin_table.restype = i32
     L.pa_rope_cos_sin_table.argtypes = [ctypes.c_double, i32, i64, vp, vp]
     L.pa_norm_rope_store_kvcache.restype = i32
@@ -133,6 +137,46 @@ def pa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stre
     _check(lib.pa_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], _ptr(k_cache),
                                 _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status), _stream(stream)),
            "pa_store_kvcache")
+
+
+def pa_prepare_prefill(seq_lens, num_cached, num_scheduled, block_table, block_size, num_blocks, max_tokens,
+                       dev_status=None, stream=None):
+    """Device-built prefill metadata.  Inputs: CUDA int32 [B] counts and the
+    [B, max_blocks] table.  Returns (cu_seqlens_q, cu_seqlens_k, positions,
+    slot_mapping, max_seqlens) as CUDA int32 tensors (positions / slots sized
+    max_tokens)."""
+    for t, n in ((seq_lens, "seq_lens"), (num_cached, "num_cached"), (num_scheduled, "num_scheduled"),
+                 (block_table, "block_table")):
+        _i32(t, n)
+    b = seq_lens.numel()
+    if num_cached.numel() != b or num_scheduled.numel() != b or block_table.dim() != 2 or block_table.shape[0] != b:
+        raise ValueError("pa_prepare_prefill: inconsistent shapes")
+    d = seq_lens.device
+    cu_q = torch.empty(b + 1, dtype=torch.int32, device=d)
+    cu_k = torch.empty(b + 1, dtype=torch.int32, device=d)
+    pos = torch.empty(max(max_tokens, 1), dtype=torch.int32, device=d)
+    sl = torch.empty(max(max_tokens, 1), dtype=torch.int32, device=d)
+    mx = torch.empty(2, dtype=torch.int32, device=d)
+    _check(lib.pa_prepare_prefill(_ptr(seq_lens), _ptr(num_cached), _ptr(num_scheduled), b, _ptr(block_table),
+                                  block_table.shape[1], block_size, num_blocks, _ptr(cu_q), _ptr(cu_k), _ptr(pos),
+                                  _ptr(sl), max_tokens, _ptr(mx), _ptr(dev_status), _stream(stream)),
+           "pa_prepare_prefill")
+    return cu_q, cu_k, pos[:max_tokens], sl[:max_tokens], mx
+
+
+def pa_prepare_decode(seq_lens, block_table, block_size, num_blocks, dev_status=None, stream=None):
+    """Device-built decode metadata: (positions, context_lens, slot_mapping), CUDA int32 [B]."""
+    _i32(seq_lens, "seq_lens")
+    _i32(block_table, "block_table")
+    b = seq_lens.numel()
+    if block_table.dim() != 2 or block_table.shape[0] != b:
+        raise ValueError("pa_prepare_decode: block_table must be [B, max_blocks]")
+    d = seq_lens.device
+    pos, ctx, sl = (torch.empty(max(b, 1), dtype=torch.int32, device=d) for _ in range(3))
+    _check(lib.pa_prepare_decode(_ptr(seq_lens), b, _ptr(block_table), block_table.shape[1], block_size, num_blocks,
+                                 _ptr(pos), _ptr(ctx), _ptr(sl), _ptr(dev_status), _stream(stream)),
+           "pa_prepare_decode")
+    return pos[:b], ctx[:b], sl[:b]
 
 
 def pa_rope_cos_sin_table(base: float, head_dim: int, max_positions: int, device=None, stream=None) -> torch.Tensor:

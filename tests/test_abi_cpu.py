@@ -145,3 +145,28 @@ def test_rope_table_host_checks(lib):
     assert f(1e6, 128, -1, FAKE, None) == 1
     assert f(1e6, 128, 0, FAKE, None) == 0    # nothing to fill
     assert f(1e6, 128, 16, None, None) == 1
+
+
+def test_metadata_host_checks(lib):
+    pf = lib.pa_prepare_prefill
+
+    def pre(sl=FAKE, nc=FAKE, ns=FAKE, b=3, bt=FAKE, mb=4, bs=16, nb=8, cq=FAKE, ck=FAKE, pos=FAKE, slots=FAKE,
+            mt=100, mx=FAKE):
+        return pf(sl, nc, ns, b, bt, mb, bs, nb, cq, ck, pos, slots, mt, mx, None, None)
+
+    assert pre(b=0) == 0
+    assert pre(b=-1) == 1
+    assert pre(sl=None) == 1
+    assert pre(mx=None) == 1
+    assert pre(mb=0) == 1
+    assert pre(nb=1 << 30, bs=256) == 1   # pool rows past int32
+    assert pre(mt=-5) == 1
+    pd = lib.pa_prepare_decode
+
+    def dec(sl=FAKE, b=3, bt=FAKE, mb=4, bs=16, nb=8, pos=FAKE, ctx=FAKE, slots=FAKE):
+        return pd(sl, b, bt, mb, bs, nb, pos, ctx, slots, None, None)
+
+    assert dec(b=0) == 0
+    assert dec(b=-2) == 1
+    assert dec(ctx=None) == 1
+    assert dec(bs=0) == 1
