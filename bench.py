@@ -431,6 +431,58 @@ def time_rope_store(device, steps, warmup, flush):
     return res
 
 
+def time_mixed(device, steps, warmup, flush):
+    """Mixed step: the 256-sequence decode batch plus one 512-token prefill
+    chunk over a 2,048-token cached prefix, as ONE prefill launch (decode rows
+    are queries of length 1) against the chunk's prefill launch followed by
+    the decode launch; L2 flushed before each timed call."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    dec = wl.decode_batch(device="cpu")
+    ctx = np.concatenate([[2048 + 512], dec.context_lens]).astype(np.int32)
+    ql = np.concatenate([[512], dec.query_lens]).astype(np.int32)
+    b = wl.paged_batch(wl.SEED_BASE + 8, ctx, ql, 256, device=device)
+    kc, vc = b.k_cache, b.v_cache
+    pa.pa_store_kvcache(b.tokens.k, b.tokens.v, kc, vc, torch.as_tensor(b.slot_mapping, device=device))
+    bt = torch.as_tensor(b.block_tables, device=device)
+    cq, ck = (torch.as_tensor(x, device=device) for x in (b.cu_seqlens_q, b.cu_seqlens_k))
+    out = torch.empty(b.tokens.q.shape, dtype=torch.bfloat16, device=device)
+    # separate launches: the chunk alone, then the 256 decode rows
+    cq1 = torch.as_tensor(np.array([0, 512], np.int32), device=device)
+    ck1 = torch.as_tensor(np.array([0, 2560], np.int32), device=device)
+    q1 = b.tokens.q[:512]
+    out1 = torch.empty(q1.shape, dtype=torch.bfloat16, device=device)
+    qd = b.tokens.q[512:]
+    ctx_d = torch.as_tensor(ctx[1:], device=device)
+    max_d = int(ctx[1:].max())
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(256, HQ, D, max_d), 256), dtype=torch.uint8, device=device)
+    outd = torch.empty((256, HQ, D), dtype=torch.bfloat16, device=device)
+
+    def mixed():
+        pa.pa_prefill_paged(b.tokens.q, cq, ck, 512, int(ctx.max()), b.scale, out, k_cache=kc, v_cache=vc,
+                            block_table=bt)
+
+    def separate():
+        pa.pa_prefill_paged(q1, cq1, ck1, 512, 2560, b.scale, out1, k_cache=kc, v_cache=vc, block_table=bt[:1])
+        pa.pa_decode_paged(qd, kc, vc, bt[1:], ctx_d, max_d, b.scale, outd, ws)
+
+    res = {}
+    for name, fn in (("one_launch", mixed), ("two_launches", separate)):
+        for _ in range(warmup):
+            fn()
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) * 1e3)
+        res[name] = {"us": statistics.median(times)}
+    res["workload"] = "256 decode rows (context U[100,1024]) + one 512-token chunk over a 2,048-token prefix"
+    return res
+
+
 def time_step_metadata(device, steps, warmup):
     """Device-built step metadata: the varlen-prefill batch (counts and tables
     of ~20 sequences, 16K tokens expanded) and a 512-sequence decode batch;
@@ -561,7 +613,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill / long-decode / CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
-    ap.add_argument("--leg", default="all", choices=["all", "prefill", "long_decode", "rope_store", "metadata"],
+    ap.add_argument("--leg", default="all",
+                    choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
     args = ap.parse_args()
@@ -581,6 +634,8 @@ def main():
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
         if args.leg == "prefill":
             res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
+        elif args.leg == "mixed":
+            res = time_mixed(device, max(args.steps, 1), args.warmup, flush)
         elif args.leg == "metadata":
             res = time_step_metadata(device, max(args.steps, 1), args.warmup)
         elif args.leg == "rope_store":
@@ -601,15 +656,35 @@ def main():
 
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) if \
         os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    # the step captured once in a CUDA graph (how a serving engine runs decode):
+    # same buffers, same kernels, no per-launch host work
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            step.run()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
     events = []
     with ClockSampler(gpu_index) as clocks:
         clocks.wait_first()
         h0 = time.time()
+        # headline: the graph replayed K times
+        g_el = time_region(graph.replay, args.steps, world)
+        # beside it: the same kernels launched one by one, with CUDA events
+        # around every decode call for the roofline
         elapsed = time_region(lambda: step.run(events), args.steps, world)
         h1 = time.time()
         time.sleep(0.3)
-    t_max, bytes_all = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
+    del graph
+    t_max, bytes_all = reduce_max_sum(world, g_el, float(step.step_bytes * args.steps))
     value = bytes_all / t_max / 1e9
+    eager_t, eager_bytes = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
+    eager_value = eager_bytes / eager_t / 1e9
     decode_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
     achieved = step.decode_bytes / decode_s / 1e9
 
@@ -634,6 +709,9 @@ def main():
         "tokens_per_s": world * step.B * args.steps / t_max,
         "hbm_frac_of_8tbs": value / 8000.0,
         "gpu_launches": args.steps * step.launches_per_step(),
+        "timing": "the 28-layer step captured once in a CUDA graph and replayed K times (how a serving engine "
+                  "runs decode); the same kernels launched one by one from Python are reported under 'eager'",
+        "eager": {"value": eager_value, "unit": "GB/s", "ms_per_step": eager_t / args.steps * 1e3},
         "e2e": {"value": e2e_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": e2e.h2d,
                 "d2h_bytes_per_step": e2e.d2h, "ms_per_step": e2e_t / args.steps * 1e3},
         "roofline": {"bound": "hbm", "kernel": "pa_decode_paged (split + merge kernels)",
@@ -664,6 +742,8 @@ def main():
             v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         line["norm_rope_store"] = rs
         line["step_metadata"] = time_step_metadata(device, max(args.steps, 5), 3)
+        torch.cuda.empty_cache()
+        line["mixed_step"] = time_mixed(device, max(args.steps, 5), 3, flush)
         import oracle
         oracle.build()
         line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)
