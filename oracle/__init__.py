@@ -83,6 +83,16 @@ def _load():
             lib.orc_rope_cos_sin.argtypes = [dbl, i32, i64, vp]
             lib.orc_rope_apply.restype = None
             lib.orc_rope_apply.argtypes = [vp, i32, vp, vp]
+            lib.orc_e4m3_value.restype = dbl
+            lib.orc_e4m3_value.argtypes = [i32]
+            lib.orc_e4m3_encode.restype = i32
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.orc_store_kvcache_fp8.restype = i32
+            lib.orc_store_kvcache_fp8.argtypes = [vp, i64, vp, i64, i64, i32, i32, ctypes.c_float, ctypes.c_float,
+                                                  vp, vp, i64, i32, vp]
+            lib.orc_decode_fp8.restype = i32
+            lib.orc_decode_fp8.argtypes = [vp, i64, vp, vp, dbl, dbl, i64, i32, vp, i32, vp, i32, i32, i32, i32, dbl,
+                                           vp]
             lib.orc_prepare_prefill.restype = i32
             lib.orc_prepare_prefill.argtypes = [vp, vp, vp, i32, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp]
             lib.orc_prepare_decode.restype = i32
@@ -283,3 +293,40 @@ def prepare_decode(seq_lens, block_table, block_size, num_blocks):
     rc = _load().orc_prepare_decode(_ptr(sl), b, _ptr(bt), bt.shape[1], block_size, num_blocks, _ptr(pos), _ptr(ctx),
                                     _ptr(slots))
     return {"positions": pos, "context_lens": ctx, "slot_mapping": slots}, rc
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one E4M3 code (NaN for 0x7f / 0xff)."""
+    return _load().orc_e4m3_value(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code of a float32 value (ties to even, saturating to +-448)."""
+    return _load().orc_e4m3_encode(float(np.float32(x)))
+
+
+def store_kvcache_fp8(k, v, k_scale, v_scale, k_cache, v_cache, slot_mapping):
+    """KV write into uint8 E4M3 pools [NB, bs, Hkv, d] (in place); returns the status."""
+    k, ks = _rows(k, "k")
+    v, vs = _rows(v, "v")
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint8 or not c.flags.c_contiguous or c.ndim != 4:
+            raise OracleError("fp8 caches: expected contiguous uint8 [NB, bs, Hkv, d]")
+    sl = _i32(slot_mapping)
+    return _load().orc_store_kvcache_fp8(_ptr(k), ks, _ptr(v), vs, k.shape[0], k.shape[1], k.shape[2],
+                                         float(k_scale), float(v_scale), _ptr(k_cache), _ptr(v_cache),
+                                         k_cache.shape[0], k_cache.shape[1], _ptr(sl))
+
+
+def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, scale):
+    """Decode over E4M3 pools; out [B, Hq, d] double."""
+    q, qs = _rows(q, "q")
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    ctx = _i32(context_lens)
+    b, hq, d = q.shape
+    out = np.zeros((b, hq, d), dtype=np.float64)
+    rc = _load().orc_decode_fp8(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale),
+                                k_cache.shape[0], k_cache.shape[1], _ptr(bt), bt.shape[1], _ptr(ctx), b, hq,
+                                k_cache.shape[2], d, float(scale), _ptr(out))
+    _check(rc, "decode_fp8")
+    return out

@@ -125,15 +125,22 @@ typedef struct {
     const uint16_t *k, *v; /* first row of the sequence in k / v */
     int64_t kv_stride;
     int kv_heads, head_dim;
+    const uint8_t *k8_cache, *v8_cache; /* fp8 (E4M3) pool instead of k_cache / v_cache, or NULL */
+    double k_scale, v_scale;            /* value = E4M3 value * scale */
 } key_source;
 
-/* Pointers to K_j and V_j for kv head g; returns 0, or ORC_BOUNDS if the table
- * entry that holds position j is not a block of the pool. */
-static int fetch_kv(const key_source *src, int64_t j, int g, const uint16_t **kj, const uint16_t **vj)
+static double e4m3_to_double(uint8_t code);
+
+/* K_j and V_j of kv head g as doubles (head_dim each); returns 0, or
+ * ORC_BOUNDS if the table entry that holds position j is not a block of the
+ * pool. */
+static int fetch_kv(const key_source *src, int64_t j, int g, double *kj, double *vj)
 {
+    const int d = src->head_dim;
     if (src->table_row == NULL) {
-        *kj = src->k + j * src->kv_stride + (int64_t)g * src->head_dim;
-        *vj = src->v + j * src->kv_stride + (int64_t)g * src->head_dim;
+        const uint16_t *kp = src->k + j * src->kv_stride + (int64_t)g * d;
+        const uint16_t *vp = src->v + j * src->kv_stride + (int64_t)g * d;
+        for (int e = 0; e < d; ++e) kj[e] = bf16_to_double(kp[e]), vj[e] = bf16_to_double(vp[e]);
         return ORC_OK;
     }
     int64_t logical_block = j / src->block_size;
@@ -141,9 +148,16 @@ static int fetch_kv(const key_source *src, int64_t j, int g, const uint16_t **kj
     int32_t phys = src->table_row[logical_block];
     if (phys < 0 || phys >= src->num_blocks) return ORC_BOUNDS;
     int64_t slot = orc_slot(src->table_row, src->block_size, j);
-    int64_t row = (slot * src->kv_heads + g) * src->head_dim;
-    *kj = src->k_cache + row;
-    *vj = src->v_cache + row;
+    int64_t row = (slot * src->kv_heads + g) * d;
+    for (int e = 0; e < d; ++e) {
+        if (src->k8_cache) {
+            kj[e] = e4m3_to_double(src->k8_cache[row + e]) * src->k_scale;
+            vj[e] = e4m3_to_double(src->v8_cache[row + e]) * src->v_scale;
+        } else {
+            kj[e] = bf16_to_double(src->k_cache[row + e]);
+            vj[e] = bf16_to_double(src->v_cache[row + e]);
+        }
+    }
     return ORC_OK;
 }
 
@@ -157,26 +171,26 @@ static int attend_row(const uint16_t *qrow, const key_source *src, int g, int64_
                       double scale, double *scores, double *out, double *weights)
 {
     const int d = src->head_dim;
+    double kj[1024], vj[1024];
     for (int e = 0; e < d; ++e) out[e] = 0.0;
     if (n_keys <= 0) return ORC_OK;
+    if (d > 1024) return ORC_INVALID;
 
     double m = -INFINITY;
     for (int64_t j = 0; j < n_keys; ++j) {
-        const uint16_t *kj, *vj;
-        if (fetch_kv(src, j, g, &kj, &vj) != ORC_OK) return ORC_BOUNDS;
+        if (fetch_kv(src, j, g, kj, vj) != ORC_OK) return ORC_BOUNDS;
         double dot = 0.0;
-        for (int e = 0; e < d; ++e) dot += bf16_to_double(qrow[e]) * bf16_to_double(kj[e]);
+        for (int e = 0; e < d; ++e) dot += bf16_to_double(qrow[e]) * kj[e];
         scores[j] = scale * dot;
         if (scores[j] > m) m = scores[j];
     }
     double denom = 0.0;
     for (int64_t j = 0; j < n_keys; ++j) denom += exp(scores[j] - m);
     for (int64_t j = 0; j < n_keys; ++j) {
-        const uint16_t *kj, *vj;
-        fetch_kv(src, j, g, &kj, &vj);
+        fetch_kv(src, j, g, kj, vj);
         double w = exp(scores[j] - m) / denom;
         if (weights) weights[j] = w;
-        for (int e = 0; e < d; ++e) out[e] += w * bf16_to_double(vj[e]);
+        for (int e = 0; e < d; ++e) out[e] += w * vj[e];
     }
     return ORC_OK;
 }
@@ -228,7 +242,7 @@ static int prefill_impl(const uint16_t *q, int64_t q_stride,
                           num_blocks, block_size, max_blocks,
                           k ? k + (int64_t)cu_k[b] * kv_stride : NULL,
                           v ? v + (int64_t)cu_k[b] * kv_stride : NULL,
-                          kv_stride, kv_heads, head_dim};
+                          kv_stride, kv_heads, head_dim, NULL, NULL, 1.0, 1.0};
         double *scores = (double *)malloc(sizeof(double) * (size_t)(lk > 0 ? lk : 1));
         for (int i = 0; i < lq; ++i) {
             const int64_t t = (int64_t)cu_q[b] + i;
@@ -281,10 +295,12 @@ int orc_prefill_weights(const uint16_t *q, int64_t q_stride,
  * query sits at position ctx-1 and sees every key.  ctx == 0 is a padded
  * row ([P1] §13.5) and yields zeros.  out is [num_seqs, Hq, d].
  */
-int orc_decode(const uint16_t *q, int64_t q_stride,
-               const uint16_t *k_cache, const uint16_t *v_cache, int64_t num_blocks, int block_size,
-               const int32_t *block_table, int max_blocks, const int32_t *context_lens,
-               int num_seqs, int num_heads, int kv_heads, int head_dim, double scale, double *out)
+static int decode_impl(const uint16_t *q, int64_t q_stride,
+                       const uint16_t *k_cache, const uint16_t *v_cache,
+                       const uint8_t *k8_cache, const uint8_t *v8_cache, double k_scale, double v_scale,
+                       int64_t num_blocks, int block_size,
+                       const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                       int num_seqs, int num_heads, int kv_heads, int head_dim, double scale, double *out)
 {
     if (check_heads(num_heads, kv_heads, head_dim) != ORC_OK) return ORC_INVALID;
     for (int b = 0; b < num_seqs; ++b)
@@ -298,7 +314,8 @@ int orc_decode(const uint16_t *q, int64_t q_stride,
         const int b = (int)(task / num_heads), h = (int)(task % num_heads);
         const int64_t ctx = context_lens[b];
         key_source src = {k_cache, v_cache, block_table + (int64_t)b * max_blocks,
-                          num_blocks, block_size, max_blocks, NULL, NULL, 0, kv_heads, head_dim};
+                          num_blocks, block_size, max_blocks, NULL, NULL, 0, kv_heads, head_dim,
+                          k8_cache, v8_cache, k_scale, v_scale};
         double *scores = (double *)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
         int rc = attend_row(q + (int64_t)b * q_stride + (int64_t)h * head_dim, &src, h / group, ctx,
                             scale, scores, out + ((int64_t)b * num_heads + h) * head_dim, NULL);
@@ -311,6 +328,95 @@ int orc_decode(const uint16_t *q, int64_t q_stride,
     return status;
 }
 
+
+int orc_decode(const uint16_t *q, int64_t q_stride,
+               const uint16_t *k_cache, const uint16_t *v_cache, int64_t num_blocks, int block_size,
+               const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+               int num_seqs, int num_heads, int kv_heads, int head_dim, double scale, double *out)
+{
+    return decode_impl(q, q_stride, k_cache, v_cache, NULL, NULL, 1.0, 1.0, num_blocks, block_size, block_table,
+                       max_blocks, context_lens, num_seqs, num_heads, kv_heads, head_dim, scale, out);
+}
+
+/* ------------------------------------------------------------------ fp8 KV cache
+ *
+ * The pages list the KV precision as a way to fit longer contexts ([P1]
+ * §17.3; [P3]'s arithmetic-intensity table counts FP8 as 1 byte per element)
+ * but fix no format.  The reading taken here: each cache element is an OCP
+ * FP8 E4M3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448), and a layer's K and V
+ * each carry one float scale: stored code = E4M3(x / scale), with the
+ * division in float (the precision of the bf16 inputs' widening) and
+ * round-to-nearest-even with saturation to +-448; value = E4M3 value * scale.
+ */
+
+/* Value of an E4M3 code. */
+static double e4m3_to_double(uint8_t code)
+{
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+double orc_e4m3_value(int code) { return e4m3_to_double((uint8_t)code); }
+
+/* Nearest E4M3 code of a float (ties to even), saturating to +-448; NaN -> 0x7f. */
+int orc_e4m3_encode(float x)
+{
+    if (isnan(x)) return 0x7f;
+    const int s = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return s | 0x7e;
+    int e2;
+    frexp(a, &e2);                         /* a = f * 2^e2, f in [0.5, 1): leading bit 2^(e2-1) */
+    if (a == 0.0 || e2 - 1 < -6) {         /* subnormal range: multiples of 2^-9 (code = k) */
+        const int k = (int)nearbyint(ldexp(a, 9));
+        return s | k;                      /* k == 8 is 2^-6, the first normal code */
+    }
+    int ex = e2 - 1;                       /* value = q * 2^(ex - 3), q in [8, 16] */
+    int q = (int)nearbyint(ldexp(a, 3 - ex));
+    if (q == 16) {
+        q = 8;
+        ++ex;
+    }
+    return s | ((ex + 7) << 3) | (q - 8);
+}
+
+/* KV write into an fp8 pool: code of float(bf16 value) / scale per element. */
+int orc_store_kvcache_fp8(const uint16_t *k, int64_t k_stride, const uint16_t *v, int64_t v_stride,
+                          int64_t num_tokens, int kv_heads, int head_dim, float k_scale, float v_scale,
+                          uint8_t *k_cache, uint8_t *v_cache, int64_t num_blocks, int block_size,
+                          const int32_t *slot_mapping)
+{
+    const int64_t row = (int64_t)kv_heads * head_dim;
+    const int64_t num_slots = num_blocks * block_size;
+    int status = ORC_OK;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        const int padding_row = slot == -1;
+        if (padding_row) continue;
+        if (slot < 0 || slot >= num_slots) { status = ORC_BOUNDS; continue; }
+        for (int64_t e = 0; e < row; ++e) {
+            const float kx = (float)bf16_to_double(k[t * k_stride + e]);
+            const float vx = (float)bf16_to_double(v[t * v_stride + e]);
+            k_cache[slot * row + e] = (uint8_t)orc_e4m3_encode(kx / k_scale);
+            v_cache[slot * row + e] = (uint8_t)orc_e4m3_encode(vx / v_scale);
+        }
+    }
+    return status;
+}
+
+/* Paged decode over an fp8 pool: as orc_decode, with K_j = E4M3 value *
+ * k_scale and V_j = E4M3 value * v_scale. */
+int orc_decode_fp8(const uint16_t *q, int64_t q_stride, const uint8_t *k_cache, const uint8_t *v_cache,
+                   double k_scale, double v_scale, int64_t num_blocks, int block_size,
+                   const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                   int num_seqs, int num_heads, int kv_heads, int head_dim, double scale, double *out)
+{
+    return decode_impl(q, q_stride, NULL, NULL, k_cache, v_cache, k_scale, v_scale, num_blocks, block_size,
+                       block_table, max_blocks, context_lens, num_seqs, num_heads, kv_heads, head_dim, scale, out);
+}
 
 /* ------------------------------------------------------------------ head norm, RoPE, KV write
  *

@@ -21,7 +21,7 @@ MUTANTS = {
     "slot_without_block_size": ("block_table_row[pos / block_size] * block_size + pos % block_size",
                                 "block_table_row[pos / block_size] + pos % block_size"),
     "unnormalised_weights": ("double w = exp(scores[j] - m) / denom;", "double w = exp(scores[j] - m);"),
-    "reads_k_for_v": ("out[e] += w * bf16_to_double(vj[e]);", "out[e] += w * bf16_to_double(kj[e]);"),
+    "reads_k_for_v": ("out[e] += w * vj[e];", "out[e] += w * kj[e];"),
     "decode_drops_new_token": ("&src, h / group, ctx,", "&src, h / group, ctx - 1,"),
     "bf16_widening_shift": ("((uint32_t)bits) << 16;", "((uint32_t)bits) << 15;"),
     "store_writes_k_to_v": ("v_cache[slot * row + e] = v[t * v_stride + e];",
@@ -45,6 +45,13 @@ MUTANTS = {
                              "if (i == end_block - 1) slot_end = base + block_size;"),
     "meta_decode_position_is_length": ("positions[b] = seqlen - 1;", "positions[b] = seqlen;"),
     "meta_decode_slot_first_block": ("block_table[(int64_t)b * max_blocks + last]", "block_table[(int64_t)b * max_blocks]"),
+    "e4m3_exponent_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_subnormal_scale": ("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)"),
+    "e4m3_ties_away": ("int q = (int)nearbyint(ldexp(a, 3 - ex));", "int q = (int)round(ldexp(a, 3 - ex));"),
+    "e4m3_no_saturation": ("if (a >= 448.0) return s | 0x7e;", "if (a >= 464.0) return s | 0x7f;"),
+    "fp8_k_scale_dropped": ("kj[e] = e4m3_to_double(src->k8_cache[row + e]) * src->k_scale;",
+                            "kj[e] = e4m3_to_double(src->k8_cache[row + e]);"),
+    "fp8_store_multiplies": ("(uint8_t)orc_e4m3_encode(kx / k_scale);", "(uint8_t)orc_e4m3_encode(kx * k_scale);"),
     "rope_before_weight": ("x[i] = bf16_to_double(double_to_bf16(yn * bf16_to_double(w_bits[i])));",
                            "x[i] = yn;"),
 }
@@ -64,6 +71,7 @@ def test_mutant_is_caught(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_norm_rope.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_metadata.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_metadata.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fp8.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
