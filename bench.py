@@ -101,10 +101,10 @@ def reduce_max_sum(world, t_max: float, units_sum: float):
 # ----------------------------------------------------------------- algorithmic counts
 
 
-def decode_bytes(ctx, block_size, num_heads=HQ, kv_heads=HKV, head_dim=D):
+def decode_bytes(ctx, block_size, num_heads=HQ, kv_heads=HKV, head_dim=D, kv_elem_bytes=2):
     """K+V rows read + q read + out written + table entries + context_lens."""
     ctx = np.asarray(ctx, dtype=np.int64)
-    kv = int(ctx.sum()) * kv_heads * head_dim * 2 * 2
+    kv = int(ctx.sum()) * kv_heads * head_dim * kv_elem_bytes * 2
     qo = len(ctx) * num_heads * head_dim * 2 * 2
     tables = int((-(-ctx // block_size)).sum()) * 4 + len(ctx) * 4
     return kv + qo + tables
@@ -386,6 +386,116 @@ def time_long_decode(device, steps, warmup, flush):
     return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512}
 
 
+def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6):
+    """The long-decode workload over fp8 (E4M3) pools: the bf16 pool's history
+    and the new tokens quantised by pa_store_kvcache_fp8, then
+    pa_decode_paged_fp8 timed with L2 flushed before each call."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    batch = wl.long_decode(device=device)
+    shape = batch.k_cache.shape
+    k8 = torch.empty(shape, dtype=torch.uint8, device=device)
+    v8 = torch.empty(shape, dtype=torch.uint8, device=device)
+    hist = wl.history_rows(batch.layout, batch.context_lens - 1)
+    rows = torch.as_tensor(hist.astype(np.int64), device=device)
+    for chunk in torch.split(rows, 1 << 18):
+        hk = batch.k_cache.view(-1, HKV, D).index_select(0, chunk)
+        hv = batch.v_cache.view(-1, HKV, D).index_select(0, chunk)
+        pa.pa_store_kvcache_fp8(hk, hv, scale, scale, k8, v8, chunk.to(torch.int32))
+    pa.pa_store_kvcache_fp8(batch.tokens.k, batch.tokens.v, scale, scale, k8, v8,
+                            torch.as_tensor(batch.slot_mapping, device=device))
+    max_ctx = int(batch.context_lens.max())
+    ctx_np = batch.context_lens
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(512, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
+    out = torch.empty((512, HQ, D), dtype=torch.bfloat16, device=device)
+    bt = torch.as_tensor(batch.block_tables, device=device)
+    ctx = torch.as_tensor(ctx_np, device=device)
+    q = batch.tokens.q
+    del batch
+    torch.cuda.empty_cache()
+
+    def run():
+        pa.pa_decode_paged_fp8(q, k8, v8, scale, scale, bt, ctx, max_ctx, wl.SCALE, out, ws)
+
+    for _ in range(warmup):
+        run()
+    times = []
+    for _ in range(steps):
+        flush_l2(flush)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        run()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) / 1e3)
+    t = statistics.median(times)
+    nbytes = decode_bytes(ctx_np, 256, kv_elem_bytes=1)
+    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512, "kv": "fp8 e4m3, scale 2^-6"}
+
+
+def time_block_size_sweep(device, steps, warmup, flush):
+    """Decode (the 256-sequence decode batch) and varlen prefill at block sizes
+    16..256: the same contexts and lengths, pools and tables rebuilt per size;
+    L2 flushed before each timed call."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    res = {"decode_gbs": {}, "prefill_tflops": {}}
+    seed = wl.SEED_BASE + 2
+    ctx = wl.rng(seed + 7).integers(100, 1024, size=256, endpoint=True)
+    lens = wl.varlen_prefill_lengths()
+    for bs in (16, 32, 64, 128, 256):
+        b = wl.paged_batch(seed, ctx, np.ones_like(ctx), bs, device=device)
+        sl = torch.as_tensor(b.slot_mapping, device=device)
+        pa.pa_store_kvcache(b.tokens.k, b.tokens.v, b.k_cache, b.v_cache, sl)
+        max_ctx = int(ctx.max())
+        ws = torch.empty(max(pa.pa_decode_workspace_bytes(256, HQ, D, max_ctx), 256), dtype=torch.uint8,
+                         device=device)
+        out = torch.empty((256, HQ, D), dtype=torch.bfloat16, device=device)
+        bt, cx = torch.as_tensor(b.block_tables, device=device), torch.as_tensor(b.context_lens, device=device)
+
+        def dec():
+            pa.pa_decode_paged(b.tokens.q, b.k_cache, b.v_cache, bt, cx, max_ctx, b.scale, out, ws)
+
+        for _ in range(warmup):
+            dec()
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            dec()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) / 1e3)
+        res["decode_gbs"][bs] = decode_bytes(ctx, bs) / statistics.median(times) / 1e9
+        del b
+        if bs in (16, 64, 256):
+            p = wl.paged_batch(wl.SEED_BASE + 3, lens, lens, bs, device=device)
+            pa.pa_store_kvcache(p.tokens.k, p.tokens.v, p.k_cache, p.v_cache,
+                                torch.as_tensor(p.slot_mapping, device=device))
+            pout = torch.empty(p.tokens.q.shape, dtype=torch.bfloat16, device=device)
+            pbt = torch.as_tensor(p.block_tables, device=device)
+            cq, ck = (torch.as_tensor(x, device=device) for x in (p.cu_seqlens_q, p.cu_seqlens_k))
+
+            def pre():
+                pa.pa_prefill_paged(p.tokens.q, cq, ck, int(lens.max()), int(lens.max()), p.scale, pout,
+                                    k_cache=p.k_cache, v_cache=p.v_cache, block_table=pbt)
+
+            for _ in range(warmup):
+                pre()
+            times = []
+            for _ in range(steps):
+                flush_l2(flush)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                pre()
+                e.record()
+                torch.cuda.synchronize()
+                times.append(s.elapsed_time(e) / 1e3)
+            res["prefill_tflops"][bs] = prefill_flops(lens, lens) / statistics.median(times) / 1e12
+            del p
+        torch.cuda.empty_cache()
+    return res
+
+
 def rope_store_bytes(num_tokens, hq=HQ, hkv=HKV):
     """Algorithmic bytes of the fused head norm + RoPE + KV write per call: the
     fused QKV row read, Q written, K and V rows written, position and slot read
@@ -614,7 +724,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
     ap.add_argument("--leg", default="all",
-                    choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed"],
+                    choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8",
+                             "block_sizes"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
     args = ap.parse_args()
@@ -634,6 +745,11 @@ def main():
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
         if args.leg == "prefill":
             res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
+        elif args.leg == "fp8":
+            res = time_long_decode_fp8(device, max(args.steps, 1), args.warmup, flush)
+            res["frac"] = res["gbs"] / peaks["hbm_gbs"]
+        elif args.leg == "block_sizes":
+            res = time_block_size_sweep(device, max(args.steps, 1), args.warmup, flush)
         elif args.leg == "mixed":
             res = time_mixed(device, max(args.steps, 1), args.warmup, flush)
         elif args.leg == "metadata":
@@ -744,6 +860,10 @@ def main():
         line["step_metadata"] = time_step_metadata(device, max(args.steps, 5), 3)
         torch.cuda.empty_cache()
         line["mixed_step"] = time_mixed(device, max(args.steps, 5), 3, flush)
+        torch.cuda.empty_cache()
+        l8 = time_long_decode_fp8(device, max(args.steps, 5), 3, flush)
+        l8["frac"] = l8["gbs"] / peaks["hbm_gbs"]
+        line["long_decode_fp8"] = l8
         import oracle
         oracle.build()
         line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)

@@ -268,6 +268,37 @@ pa_status pa_decode_paged(const void *q, int64_t q_stride_seq,
                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * fp8 KV cache ("大模型推理入门与 nano-vLLM 源码详解" §17.3 names the KV
+ * precision as the lever for longer contexts; "VLLM on Fain的Blog" counts FP8
+ * at one byte per element.  The pages fix no format; this library's is the
+ * OCP FP8 E4M3 format with one float scale per layer for K and one for V).
+ *
+ * pa_store_kvcache_fp8: as pa_store_kvcache, but pool element e receives the
+ * E4M3 code of float(x) / scale (division in fp32, round to nearest even,
+ * saturating to +-448; NaN stays NaN).  k_cache / v_cache are
+ * [num_blocks, block_size, num_kv_heads, head_dim] bytes.  Scales must be
+ * positive and finite.  k, v and the caches must be 16-byte aligned and the
+ * token strides multiples of 8.  The codes are deterministic (bit-exact).
+ */
+pa_status pa_store_kvcache_fp8(const void *k, int64_t k_stride_tok, const void *v, int64_t v_stride_tok,
+                               int64_t num_tokens, int num_kv_heads, int head_dim, float k_scale, float v_scale,
+                               void *k_cache, void *v_cache, int64_t num_blocks, int block_size,
+                               const int32_t *slot_mapping, int32_t *dev_status, void *stream);
+
+/*
+ * pa_decode_paged_fp8: pa_decode_paged over fp8 pools written by
+ * pa_store_kvcache_fp8, with K_j = E4M3 value * k_scale and V_j = E4M3 value *
+ * v_scale.  Same arguments, workspace (pa_decode_workspace_bytes) and errors
+ * as pa_decode_paged; half the bytes per context token.
+ */
+pa_status pa_decode_paged_fp8(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
+                              float k_scale, float v_scale, int64_t num_blocks, int block_size,
+                              const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+                              int num_seqs, int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                              float scale, void *out, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, void *stream);
+
+/*
  * Paged decode for callers that cannot allocate device memory.  (The pages
  * describe no counterpart: this is a calling convention of this library.)
  *

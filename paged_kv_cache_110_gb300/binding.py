@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
-    "pa_store_kvcache", "pa_prepare_prefill", "pa_prepare_decode", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
+    "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_decode_paged_fp8", "pa_prepare_prefill", "pa_prepare_decode", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
     "pa_decode_paged_noalloc",
 ]
 
@@ -44,6 +44,11 @@ def _load() -> ctypes.CDLL:
     L.pa_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
     L.pa_store_kvcache.restype = i32
     L.pa_store_kvcache.argtypes = [vp, i64, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_store_kvcache_fp8.restype = i32
+    L.pa_store_kvcache_fp8.argtypes = [vp, i64, vp, i64, i64, i32, i32, f32, f32, vp, vp, i64, i32, vp, vp, vp]
+    L.pa_decode_paged_fp8.restype = i32
+    L.pa_decode_paged_fp8.argtypes = [vp, i64, vp, vp, f32, f32, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32,
+                                      vp, vp, sz, vp, vp]
     L.pa_prepare_prefill.restype = i32
     L.pa_prepare_prefill.argtypes = [vp, vp, vp, i32, vp, i32, i32, i64, vp, vp, vp, vp, i64, vp, vp, vp]
     L.pa_prepare_decode.restype = i32
@@ -137,6 +142,46 @@ def pa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stre
     _check(lib.pa_store_kvcache(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], _ptr(k_cache),
                                 _ptr(v_cache), nb, bs, _ptr(slot_mapping), _ptr(dev_status), _stream(stream)),
            "pa_store_kvcache")
+
+
+def _cache8(t: torch.Tensor, name: str):
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 4 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA uint8 / float8_e4m3fn [num_blocks, block_size, Hkv, D]")
+    return t.shape
+
+
+def pa_store_kvcache_fp8(k, v, k_scale, v_scale, k_cache, v_cache, slot_mapping, dev_status=None, stream=None):
+    """KV write into E4M3 pools: k, v [T, Hkv, 128] bf16 views; caches uint8 [NB, bs, Hkv, 128]."""
+    hkv, ks = _bf16_rows(k, "k")
+    _, vs = _bf16_rows(v, "v")
+    nb, bs, chk, _ = _cache8(k_cache, "k_cache")
+    _cache8(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    if slot_mapping.numel() != k.shape[0] or v.shape[0] != k.shape[0] or chk != hkv:
+        raise ValueError("pa_store_kvcache_fp8: inconsistent shapes")
+    _check(lib.pa_store_kvcache_fp8(_ptr(k), ks, _ptr(v), vs, k.shape[0], hkv, k.shape[2], float(k_scale),
+                                    float(v_scale), _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(slot_mapping),
+                                    _ptr(dev_status), _stream(stream)),
+           "pa_store_kvcache_fp8")
+
+
+def pa_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, max_context_len, scale, out,
+                        workspace, dev_status=None, stream=None):
+    """Paged decode over E4M3 pools (see pa_decode_paged for the other arguments)."""
+    hq, qs = _bf16_rows(q, "q")
+    nb, bs, hkv, d = _cache8(k_cache, "k_cache")
+    _cache8(v_cache, "v_cache")
+    _i32(block_table, "block_table")
+    _i32(context_lens, "context_lens")
+    b = q.shape[0]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (b, hq, d):
+        raise ValueError("out must be a contiguous bf16 [B, Hq, D] tensor")
+    _check(lib.pa_decode_paged_fp8(_ptr(q), qs, _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale), nb,
+                                   bs, _ptr(block_table), block_table.shape[1], _ptr(context_lens), b,
+                                   int(max_context_len), hq, hkv, d, float(scale), _ptr(out), _ptr(workspace),
+                                   workspace.numel() if workspace is not None else 0, _ptr(dev_status),
+                                   _stream(stream)),
+           "pa_decode_paged_fp8")
 
 
 def pa_prepare_prefill(seq_lens, num_cached, num_scheduled, block_table, block_size, num_blocks, max_tokens,

@@ -27,6 +27,9 @@
 //  * Splits with more than one part write fp32 partials to the workspace and
 //    a small merge kernel combines them; a single-split sequence is
 //    finalised in place.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <cstdlib>
 #include <mutex>
 
@@ -43,8 +46,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 struct DecodeParams {
     const uint16_t *q;
     int64_t q_stride;
-    const uint16_t *k_cache;
-    const uint16_t *v_cache;
+    const void *k_cache;  // bf16, or E4M3 codes (fp8 pools)
+    const void *v_cache;
     int64_t num_blocks;
     int block_size;
     const int32_t *block_table;
@@ -54,7 +57,8 @@ struct DecodeParams {
     int max_ctx;
     int num_heads;
     int kv_heads;
-    float scale_log2;
+    float scale_log2;   // scale * log2(e) (times the K scale for fp8 pools)
+    float out_scale;    // 1, or the V scale for fp8 pools
     uint16_t *out;
     float *ws_o;      // [num_seqs][max_splits][num_heads][D]
     float2 *ws_ml;    // [num_seqs][max_splits][num_heads] (max, sum), base-2
@@ -105,6 +109,45 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
     f[6] = pa::bf16_lo(u.w); f[7] = pa::bf16_hi(u.w);
 }
 
+// 8 E4M3 codes (little-endian in u) to floats, exactly (through f16).
+__device__ __forceinline__ void unpack8(const uint2 &u, float (&f)[8])
+{
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w[i] >> (16 * j)), __NV_E4M3);
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+            f[4 * i + 2 * j] = v.x;
+            f[4 * i + 2 * j + 1] = v.y;
+        }
+    }
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const void *p)
+{
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// The pool's element type: bf16 rows (16 bytes per lane load) or E4M3 rows (8).
+template <bool FP8>
+struct KvRow {
+    using Raw = uint4;
+    using Elem = uint16_t;
+    static __device__ __forceinline__ Raw load(const Elem *p) { return pa::ld_stream16(p); }
+    static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
+};
+template <>
+struct KvRow<true> {
+    using Raw = uint2;
+    using Elem = uint8_t;
+    static __device__ __forceinline__ Raw load(const Elem *p) { return ld_stream8(p); }
+    static __device__ __forceinline__ Raw zero() { return make_uint2(0, 0); }
+};
+
 // One transposing butterfly step over the 16 lanes of a half-warp: lanes
 // whose bit M is set keep the upper half of x, the others the lower half,
 // and each adds its partner's copy of the half it keeps.  With N == 1 it is
@@ -139,9 +182,10 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-template <int G>
+template <int G, bool FP8>
 __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
 {
+    using KV = KvRow<FP8>;
     constexpr int V = 8 * G;                 // partial dot products per lane per chunk
     constexpr int R = V >= 16 ? V / 16 : 1;  // whole dot products per lane after the butterfly
     const int b = blockIdx.x, s = blockIdx.y;
@@ -197,19 +241,19 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
         // a chunk never crosses a block: cb and block_size are multiples of 16
         const int64_t row0 = int64_t(phys) * p.block_size + (cb % p.block_size) + half * 8;
-        const uint16_t *kp = p.k_cache + row0 * row_elems + g * D + 8 * c;
-        const uint16_t *vp = p.v_cache + row0 * row_elems + g * D + 8 * c;
+        const typename KV::Elem *kp = static_cast<const typename KV::Elem *>(p.k_cache) + row0 * row_elems + g * D + 8 * c;
+        const typename KV::Elem *vp = static_cast<const typename KV::Elem *>(p.v_cache) + row0 * row_elems + g * D + 8 * c;
         const int nvalid = t1 - (cb + half * 8);  // tokens of this half inside the split
 
-        uint4 kr[8], vr[8];
+        typename KV::Raw kr[8], vr[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (i < nvalid) {
-                kr[i] = pa::ld_stream16(kp + i * row_elems);
-                vr[i] = pa::ld_stream16(vp + i * row_elems);
+                kr[i] = KV::load(kp + i * row_elems);
+                vr[i] = KV::load(vp + i * row_elems);
             } else {
-                kr[i] = make_uint4(0, 0, 0, 0);
-                vr[i] = make_uint4(0, 0, 0, 0);
+                kr[i] = KV::zero();
+                vr[i] = KV::zero();
             }
         }
 
@@ -327,7 +371,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     if (nsplit == 1) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float inv = 1.f / l[h];
+            const float inv = p.out_scale / l[h];
             uint4 u;
             u.x = pa::pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
             u.y = pa::pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
@@ -374,7 +418,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
             acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
             acc[4] += bb.x * w; acc[5] += bb.y * w; acc[6] += bb.z * w; acc[7] += bb.w * w;
         }
-        const float inv = 1.f / ll;
+        const float inv = p.out_scale / ll;
         uint4 u;
         u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
         u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
@@ -384,11 +428,11 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     }
 }
 
-template <int G>
+template <int G, bool FP8>
 void launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
-    decode_split_kernel<G><<<grid, NW * 32, 0, stream>>>(p);
+    decode_split_kernel<G, FP8><<<grid, NW * 32, 0, stream>>>(p);
 }
 
 pa_status check_args(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
@@ -418,12 +462,13 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int hea
     return workspace_bytes(num_seqs, num_heads, make_plan(num_seqs, max_context_len));
 }
 
-extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
-                                     int64_t num_blocks, int block_size, const int32_t *block_table,
-                                     int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                                     int max_context_len, int num_heads, int num_kv_heads, int head_dim,
-                                     float scale, void *out, void *workspace, size_t workspace_bytes_given,
-                                     int32_t *dev_status, void *stream)
+namespace {
+
+pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache, bool fp8,
+                      float k_scale, float v_scale, int64_t num_blocks, int block_size, const int32_t *block_table,
+                      int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int max_context_len,
+                      int num_heads, int num_kv_heads, int head_dim, float scale, void *out, void *workspace,
+                      size_t workspace_bytes_given, int32_t *dev_status, void *stream)
 {
     pa_status st = check_args(q, q_stride_seq, k_cache, v_cache, num_blocks, block_size, block_table,
                               max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
@@ -438,8 +483,8 @@ extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const 
     DecodeParams p;
     p.q = static_cast<const uint16_t *>(q);
     p.q_stride = q_stride_seq;
-    p.k_cache = static_cast<const uint16_t *>(k_cache);
-    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
     p.num_blocks = num_blocks;
     p.block_size = block_size;
     p.block_table = block_table;
@@ -449,7 +494,8 @@ extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const 
     p.max_ctx = max_context_len;
     p.num_heads = num_heads;
     p.kv_heads = num_kv_heads;
-    p.scale_log2 = scale * LOG2E;
+    p.scale_log2 = scale * LOG2E * k_scale;
+    p.out_scale = v_scale;
     p.out = static_cast<uint16_t *>(out);
     const size_t n = size_t(num_seqs) * (plan.max_splits > 0 ? plan.max_splits : 1) * num_heads;
     p.ws_o = static_cast<float *>(workspace);
@@ -461,14 +507,55 @@ extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const 
     p.status = dev_status;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (num_heads / num_kv_heads) {
-    case 1: launch_split<1>(p, s); break;
-    case 2: launch_split<2>(p, s); break;
-    case 4: launch_split<4>(p, s); break;
-    default: launch_split<8>(p, s); break;
+    const int group = num_heads / num_kv_heads;
+    if (fp8) {
+        switch (group) {
+        case 1: launch_split<1, true>(p, s); break;
+        case 2: launch_split<2, true>(p, s); break;
+        case 4: launch_split<4, true>(p, s); break;
+        default: launch_split<8, true>(p, s); break;
+        }
+    } else {
+        switch (group) {
+        case 1: launch_split<1, false>(p, s); break;
+        case 2: launch_split<2, false>(p, s); break;
+        case 4: launch_split<4, false>(p, s); break;
+        default: launch_split<8, false>(p, s); break;
+        }
     }
     if (plan.max_splits > 1) decode_merge_kernel<<<dim3(unsigned(num_seqs)), 256, 0, s>>>(p);
     return pa::launch_status();
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
+                                     int64_t num_blocks, int block_size, const int32_t *block_table,
+                                     int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                     int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                                     float scale, void *out, void *workspace, size_t workspace_bytes_given,
+                                     int32_t *dev_status, void *stream)
+{
+    return decode_impl(q, q_stride_seq, k_cache, v_cache, false, 1.f, 1.f, num_blocks, block_size, block_table,
+                       max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                       head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream);
+}
+
+// Decode over fp8 (E4M3) pools written by pa_store_kvcache_fp8: the same
+// kernel reading 1-byte elements (half the bytes per context token), with K
+// scaled inside the score and V scaled once at the output.
+extern "C" pa_status pa_decode_paged_fp8(const void *q, int64_t q_stride_seq, const void *k_cache,
+                                         const void *v_cache, float k_scale, float v_scale, int64_t num_blocks,
+                                         int block_size, const int32_t *block_table, int max_blocks_per_seq,
+                                         const int32_t *context_lens, int num_seqs, int max_context_len,
+                                         int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
+                                         void *workspace, size_t workspace_bytes_given, int32_t *dev_status,
+                                         void *stream)
+{
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || isinf(k_scale) || isinf(v_scale)) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, q_stride_seq, k_cache, v_cache, true, k_scale, v_scale, num_blocks, block_size,
+                       block_table, max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
+                       num_kv_heads, head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------
