@@ -52,8 +52,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 # DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
 # valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha256": "f1b8af4f9bd84c0ce98c0ef90dd4132dea8a05a981cce4fd992a1eb071e7c644",
-               "bytes_per_call": 586_690_304 + 5_865_216, "kernel": "decode_split_kernel<2>"}
+NCU_TRAFFIC = {"source_sha256": "801c3ef5949195749c03b084d59957067da366c71c2ebdbe1856062a6e4dcfe8",
+               "bytes_per_call": 586_680_832 + 5_629_696, "kernel": "decode_split_kernel<2, 0>"}
 
 
 def _file_sha(path):
