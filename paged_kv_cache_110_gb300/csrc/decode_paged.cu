@@ -34,12 +34,14 @@
 #include <mutex>
 
 #include "pa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace {
 
 constexpr int D = pa::kHeadDim;
 constexpr int NW = 8;          // warps per CTA
 constexpr int CHUNK = 16;      // tokens per warp iteration (8 per half-warp)
+constexpr int PREFETCH_CHUNKS = 1;  // how many of a warp's chunks ahead to prefetch into L2
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -244,6 +246,21 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         const typename KV::Elem *kp = static_cast<const typename KV::Elem *>(p.k_cache) + row0 * row_elems + g * D + 8 * c;
         const typename KV::Elem *vp = static_cast<const typename KV::Elem *>(p.v_cache) + row0 * row_elems + g * D + 8 * c;
         const int nvalid = t1 - (cb + half * 8);  // tokens of this half inside the split
+        if (PREFETCH_CHUNKS > 0 && g == 0 && lane == 0) {
+            // bring a later chunk of this warp's sequence of chunks into L2: its
+            // 16 token rows of all KV heads are one contiguous run of one block
+            const int cn = cb + PREFETCH_CHUNKS * wph * CHUNK;
+            if (cn < t1) {
+                const int32_t pn = table[cn / p.block_size];
+                if (pn >= 0 && int64_t(pn) < p.num_blocks) {
+                    const int64_t r = (int64_t(pn) * p.block_size + cn % p.block_size) * row_elems;
+                    const uint32_t bytes = uint32_t(min(CHUNK, t1 - cn) * row_elems * sizeof(typename KV::Elem));
+                    const uint32_t b16 = (bytes + 15u) & ~15u;
+                    pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.k_cache) + r, b16);
+                    pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.v_cache) + r, b16);
+                }
+            }
+        }
 
         typename KV::Raw kr[8], vr[8];
 #pragma unroll

@@ -266,6 +266,13 @@ __device__ __forceinline__ void tmem_st64_sync(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
+// Ask for `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address to be brought into L2, without waiting or touching registers.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------ registers
 
 // Move registers between the warpgroups of a CTA: every warp of a warpgroup
