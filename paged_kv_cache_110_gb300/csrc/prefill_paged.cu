@@ -426,8 +426,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         src.box_rows = p.box_rows;
         src.block_size = p.block_size;
         if (lane == 0) tma_prefetch_desc(src.map);
-        constexpr int nst = KSTAGES;
-        static_assert(KSTAGES == VSTAGES, "one stage count for both producers");
+        const int nst = is_k ? KSTAGES : VSTAGES;
         const uint32_t base = sb + (is_k ? OFF_K : OFF_V);
         const int full0 = is_k ? B_KF : B_VF, empty0 = is_k ? B_KE : B_VE;
         int t = 0;  // tiles issued
