@@ -320,6 +320,10 @@ def time_prefill(device, steps, warmup, flush, only="all"):
     if only in ("all", "prefix_2048_chunked"):
         a, b, _ = wl.prefix_chunk(device=device)
         cases["prefix_2048_chunked"] = [a, b]
+    if only in ("all", "chunk_512_over_8k"):
+        # one long prompt's chunk: 512 new tokens over 7,680 cached ones (few
+        # work items: the key range of each is split over several CTAs)
+        cases["chunk_512_over_8k"] = [wl.paged_batch(wl.SEED_BASE + 9, [8192], [512], 256, device=device)]
     for name, calls in cases.items():
         kc, vc = calls[0].k_cache, calls[0].v_cache
         prepared = []
@@ -332,14 +336,18 @@ def time_prefill(device, steps, warmup, flush, only="all"):
                              torch.as_tensor(c.cu_seqlens_k, device=device)))
             flops += prefill_flops(c.query_lens, c.context_lens)
 
+        wss = [torch.empty(max(pa.pa_prefill_workspace_bytes(c.layout.num_seqs, int(c.query_lens.max()),
+                                                              int(c.context_lens.max()), HQ, HKV), 256),
+                           dtype=torch.uint8, device=device) for c in calls]
+
         def run(ev=None):
-            for c, out, sl, bt, cq, ck in prepared:
+            for (c, out, sl, bt, cq, ck), ws in zip(prepared, wss):
                 pa.pa_store_kvcache(c.tokens.k, c.tokens.v, kc, vc, sl)
                 if ev is not None:
                     ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                     ev[-1][0].record()
                 pa.pa_prefill_paged(c.tokens.q, cq, ck, int(c.query_lens.max()), int(c.context_lens.max()),
-                                    c.scale, out, k_cache=kc, v_cache=vc, block_table=bt)
+                                    c.scale, out, k_cache=kc, v_cache=vc, block_table=bt, workspace=ws)
                 if ev is not None:
                     ev[-1][1].record()
 
@@ -727,7 +735,8 @@ def main():
                     choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8",
                              "block_sizes"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
-    ap.add_argument("--prefill-case", default="all", choices=["all", "varlen_16k", "prefix_2048_chunked"])
+    ap.add_argument("--prefill-case", default="all",
+                    choices=["all", "varlen_16k", "prefix_2048_chunked", "chunk_512_over_8k"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -219,15 +219,26 @@ pa_status pa_prepare_decode(const int32_t *seq_lens, int num_seqs, const int32_t
  *                 PA_ERR_BOUNDS and its rows beyond the bound are not computed.
  *   scale         softmax scale applied to q.k (1/sqrt(head_dim) usually).
  *   out           [Tq, num_heads, head_dim] bf16, packed.
+ *   workspace     device scratch of pa_prefill_workspace_bytes(num_seqs,
+ *                 max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads) bytes,
+ *                 256-byte aligned (NULL when that is 0); its contents on entry
+ *                 do not matter.  A call with fewer (query tile pair, KV head)
+ *                 items than fill the GPU twice splits each item's keys into
+ *                 ranges computed by different CTAs and merges their softmax
+ *                 statistics exactly (§9.5); the workspace holds the shares.
+ *                 Calls that overlap on the GPU must not share a workspace.
  * Sequences with Lq_b == 0 are skipped.  Lk_b < Lq_b sets PA_ERR_INVALID_ARG.
  */
+size_t pa_prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads);
+
 pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64_t num_tokens,
                            const void *k, const void *v, int64_t kv_stride_tok,
                            const void *k_cache, const void *v_cache, int64_t num_blocks, int block_size,
                            const int32_t *block_table, int max_blocks_per_seq,
                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int num_seqs,
                            int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
-                           int head_dim, float scale, void *out, int32_t *dev_status, void *stream);
+                           int head_dim, float scale, void *out, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_status, void *stream);
 
 /*
  * Bytes of scratch pa_decode_paged needs for these host-side sizes on the

@@ -17,8 +17,9 @@ from . import _build
 
 __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
-    "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_decode_paged_fp8", "pa_prepare_prefill", "pa_prepare_decode", "pa_rope_cos_sin_table", "pa_norm_rope_store_kvcache", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_decode_paged",
-    "pa_decode_paged_noalloc",
+    "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_norm_rope_store_kvcache", "pa_rope_cos_sin_table",
+    "pa_prepare_prefill", "pa_prepare_decode", "pa_prefill_workspace_bytes", "pa_prefill_paged",
+    "pa_decode_workspace_bytes", "pa_decode_paged", "pa_decode_paged_fp8", "pa_decode_paged_noalloc",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
@@ -60,7 +61,9 @@ def _load() -> ctypes.CDLL:
                                              i64, i32, vp, vp, vp]
     L.pa_prefill_paged.restype = i32
     L.pa_prefill_paged.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, i32, i32, i32,
-                                   i32, i32, i32, f32, vp, vp, vp]
+                                   i32, i32, i32, f32, vp, vp, sz, vp, vp]
+    L.pa_prefill_workspace_bytes.restype = sz
+    L.pa_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.pa_decode_workspace_bytes.restype = sz
     L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.pa_decode_paged.restype = i32
@@ -265,10 +268,16 @@ def pa_norm_rope_store_kvcache(qkv, num_heads, num_kv_heads, positions, cos_sin,
            "pa_norm_rope_store_kvcache")
 
 
+def pa_prefill_workspace_bytes(num_seqs, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads) -> int:
+    return lib.pa_prefill_workspace_bytes(num_seqs, int(max_seqlen_q), int(max_seqlen_k), num_heads, num_kv_heads)
+
+
 def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, out, *, k=None, v=None,
-                     k_cache=None, v_cache=None, block_table=None, dev_status=None, stream=None):
+                     k_cache=None, v_cache=None, block_table=None, workspace=None, dev_status=None, stream=None):
     """Causal varlen prefill.  With block_table=None keys come from k/v;
-    otherwise from the paged caches."""
+    otherwise from the paged caches.  workspace: a CUDA uint8 tensor of at
+    least pa_prefill_workspace_bytes(...) bytes; when None and one is needed,
+    it is allocated here (through PyTorch's allocator)."""
     hq, qs = _bf16_rows(q, "q")
     if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (q.shape[0], hq, q.shape[2]):
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
@@ -290,9 +299,13 @@ def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
         if block_table.dim() != 2 or block_table.shape[0] != nseq:
             raise ValueError("block_table must be [num_seqs, max_blocks]")
         args = (None, None, 0, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table), block_table.shape[1])
+    need = lib.pa_prefill_workspace_bytes(nseq, int(max_seqlen_q), int(max_seqlen_k), hq, hkv) if nseq > 0 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(lib.pa_prefill_paged(_ptr(q), qs, q.shape[0], *args, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
                                 int(max_seqlen_q), int(max_seqlen_k), hq, hkv, q.shape[2], float(scale), _ptr(out),
-                                _ptr(dev_status), _stream(stream)),
+                                _ptr(workspace), 0 if workspace is None else workspace.numel(), _ptr(dev_status),
+                                _stream(stream)),
            "pa_prefill_paged")
 
 

@@ -45,6 +45,7 @@
 // what it issued, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -93,7 +94,7 @@ enum {
 constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA thread, softmax warps
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag
 constexpr int OFF_RING = OFF_MISC + 16;           // the item ring (RingSlot x RING)
-constexpr int RING_SLOT_BYTES = 80;
+constexpr int RING_SLOT_BYTES = 96;
 constexpr int TABLE_SMEM = 256;                   // block ids staged per item (more: read from global)
 constexpr int OFF_TABLE = OFF_RING + RING * RING_SLOT_BYTES;  // two buffers
 constexpr int SMEM_BYTES = OFF_TABLE + 2 * TABLE_SMEM * 4;  // the base is 1024-byte aligned (checked)
@@ -130,6 +131,9 @@ struct TcParams {
     uint16_t *out;
     int32_t *status;
     unsigned int sched_slot;  // which scheduler counter pair this call uses
+    int kv_splits;            // key ranges per item (1: no split); split items write partials
+    float *ws_o;              // [unit][QT][BM][D] unnormalised O of split items
+    float2 *ws_ml;            // [unit][QT][BM] (running max in scaled log2 units, exponent sum)
 };
 
 // Work-item counters, one pair [next item, CTAs finished] per call in flight.
@@ -143,21 +147,33 @@ __device__ unsigned int g_prefill_sched[SCHED_SLOTS][2];
 // Parity of completion number n of a barrier used by every nbuf-th round.
 __device__ __forceinline__ uint32_t par(int n, int nbuf) { return uint32_t(n / nbuf) & 1u; }
 
-// One work item: two 128-row query tiles of one sequence that read the same
-// KV head.  A tile with rows == 0 is empty (nt == 0).
+// One work unit: the K/V tiles jb .. jb+nmax-1 of an item, which is two
+// 128-row query tiles of one sequence that read the same KV head.  nt[a] counts
+// query tile a's tiles in this unit (0: nothing to do for it).  When an item's
+// keys are split over several units (split), each unit's softmax statistics
+// and unnormalised O go to the workspace and a merge kernel combines them
+// exactly ("大模型推理入门与 nano-vLLM 源码详解" §9.5).
 struct Item {
     int b, g, q0, k0, offset;
     int h[QT], m0[QT], rows[QT], kend[QT], nt[QT];
-    int nmax, kend_max;  // K/V tiles and keys the item reads
-    bool valid, bad;
+    int nmax, kend_max;  // K/V tiles of the unit; keys the item reads
+    int jb;              // first K/V tile of the unit
+    bool valid, bad, split, last;
     int bad_code;
 };
 
-// Items are numbered so that consecutive numbers walk (unit, sequence) and
-// then the step from the last one down: the heaviest tiles come first.
+// Units are numbered item-major with the key split innermost; items walk
+// (unit, sequence) and then the step from the last one down, so the heaviest
+// tiles come first.
+template <bool SPLIT>
 __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
 {
     Item it;
+    int ks = 0;
+    if (SPLIT) {
+        ks = w % p.kv_splits;
+        w /= p.kv_splits;
+    }
     const int xb = p.units * p.num_seqs;
     const int y = w / xb, x = w % xb;
     const int u = x % p.units;
@@ -189,7 +205,20 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int w)
         it.kend_max = max(it.kend_max, it.kend[a]);
     }
     it.g = it.h[0] / (p.num_heads / p.kv_heads);
-    it.valid = it.rows[0] > 0 && !it.bad;
+    it.jb = 0;
+    it.split = false;
+    it.last = true;
+    if (SPLIT) {  // this unit's share of the item's K/V tiles
+        const int per = (it.nmax + p.kv_splits - 1) / p.kv_splits;
+        it.jb = ks * per;
+        const int je = min(it.nmax, it.jb + per);
+        it.split = per < it.nmax;
+        it.last = je == it.nmax;
+#pragma unroll
+        for (int a = 0; a < QT; ++a) it.nt[a] = max(0, min(je, it.nt[a]) - it.jb);
+        it.nmax = max(0, je - it.jb);
+    }
+    it.valid = it.rows[0] > 0 && !it.bad && it.nmax > 0;
     if (lq > p.max_q && !it.bad) {
         it.bad = true;
         it.bad_code = PA_ERR_BOUNDS;
@@ -264,6 +293,7 @@ __device__ __forceinline__ void mask_tail(uint32_t (&s)[N], int base, int limit)
         if (base + c > limit) s[c] = NEG_INF_BITS;
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -280,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         return;
     }
     const bool paged = p.block_table != nullptr;
-    const int n_items = p.n_steps * p.units * p.num_seqs;
+    const int n_items = p.n_steps * p.units * p.num_seqs * p.kv_splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < QSLOTS; ++s) {
@@ -354,7 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 if (lane == 0) cand = int(atomicAdd(&g_prefill_sched[p.sched_slot][0], 1u));
                 cand = __shfl_sync(FULL, cand, 0);
                 if (cand >= n_items) break;
-                const Item it = decode_item(p, cand);
+                const Item it = decode_item<SPLIT>(p, cand);
                 if (it.bad && lane == 0) pa::report(p.status, it.bad_code);
                 if (it.valid) {
                     w = cand;
@@ -367,7 +397,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 break;
             Item it;
             if (w >= 0) {
-                it = decode_item(p, w);
+                it = decode_item<SPLIT>(p, w);
                 if (n >= 2 && !__all_sync(FULL, mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)))
                     break;
                 if (paged) {
@@ -447,8 +477,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 const int st = t % nst;
                 if (t >= nst && !(ok = mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, WAIT_LIMIT)))
                     break;
-                load_tile(src, it.g * D, j * BN, it.kend_max, base + st * TILE_BYTES, bar(full0 + st), lane,
-                          p.num_blocks);
+                load_tile(src, it.g * D, ((SPLIT ? it.jb : 0) + j) * BN, it.kend_max, base + st * TILE_BYTES,
+                          bar(full0 + st), lane, p.num_blocks);
             }
             if (!ok) break;
             if (lane == 0) mbar_arrive(bar(B_TE + tb));  // this producer no longer reads the block ids
@@ -583,7 +613,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             // pool slots (any bits) or another sequence's rows: the warpgroup of
             // the first query tile that reads that tile sets those V rows to 0
             // so that 0 * V stays 0
-            const bool zeroer = a == (it.nt[0] == it.nmax ? 0 : 1) && it.kend_max < it.nmax * BN;
+            const int jb = SPLIT ? it.jb : 0;  // first K/V tile of the unit
+            const bool zeroer = a == (it.nt[0] == it.nmax ? 0 : 1) && (!SPLIT || it.last) &&
+                                it.kend_max < (jb + it.nmax) * BN;
             const int pos = it.offset + it.m0[a] + r;
             const int last_visible = min(pos, it.kend[a] - 1);
             float m_used = -INFINITY;  // running max in scaled base-2 units
@@ -592,7 +624,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 ok = __all_sync(FULL, mbar_wait(bar(B_SF + a), uint32_t(c) & 1u, abort_flag, WAIT_LIMIT));
                 if (!ok) break;
                 tc_fence_after();
-                const int j0 = j * BN;
+                const int j0 = (jb + j) * BN;
                 const bool masked = j0 + BN - 1 > it.offset + it.m0[a];  // the tile crosses some row's causal bound
                 const int limit = last_visible - j0;
                 // pass 1: row max of the raw scores
@@ -674,6 +706,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             ++no;
             if (!ok) break;
             tc_fence_after();
+            if (SPLIT && it.split) {
+                // a share of a split item: unnormalised O and (max, sum) for the merge
+                const int64_t row = (int64_t(w) * QT + a) * BM + r;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t o[64];
+                    tmem_ld64_sync(ocol + hf * 64, o);
+                    if (r < it.rows[a]) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + row * D + hf * 64);
+#pragma unroll
+                        for (int v = 0; v < 16; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                                 __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                    }
+                }
+                if (r < it.rows[a]) p.ws_ml[row] = make_float2(m_used, l);
+                continue;
+            }
             const float inv = 1.f / l;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -714,6 +764,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     }
 }
 
+// Combine the key-range shares of every split item: per query row,
+// M = max_s m_s, L = sum_s l_s 2^(m_s - M), out = sum_s O_s 2^(m_s - M) / L
+// ("大模型推理入门与 nano-vLLM 源码详解" §9.5).  A CTA per (item, query tile), a
+// thread per row.
+__global__ void __launch_bounds__(BM) prefill_merge_kernel(const __grid_constant__ TcParams p)
+{
+    const int a = blockIdx.y, r = threadIdx.x;
+    const int w0 = blockIdx.x * p.kv_splits;
+    const Item first = decode_item<true>(p, w0);
+    if (!first.split || first.bad || r >= first.rows[a]) return;
+    float mm = -INFINITY;
+    for (int s = 0; s < p.kv_splits; ++s) {
+        const Item it = decode_item<true>(p, w0 + s);
+        if (it.valid && it.nt[a] > 0) mm = fmaxf(mm, p.ws_ml[(int64_t(w0 + s) * QT + a) * BM + r].x);
+    }
+    float acc[D];
+#pragma unroll
+    for (int e = 0; e < D; ++e) acc[e] = 0.f;
+    float ll = 0.f;
+    for (int s = 0; s < p.kv_splits; ++s) {
+        const Item it = decode_item<true>(p, w0 + s);
+        if (!it.valid || it.nt[a] == 0) continue;
+        const int64_t row = (int64_t(w0 + s) * QT + a) * BM + r;
+        const float2 ml = p.ws_ml[row];
+        const float wgt = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - mm);
+        ll = fmaf(ml.y, wgt, ll);
+        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * D);
+#pragma unroll
+        for (int v = 0; v < D / 4; ++v) {
+            const float4 x = src[v];
+            acc[4 * v] = fmaf(x.x, wgt, acc[4 * v]);
+            acc[4 * v + 1] = fmaf(x.y, wgt, acc[4 * v + 1]);
+            acc[4 * v + 2] = fmaf(x.z, wgt, acc[4 * v + 2]);
+            acc[4 * v + 3] = fmaf(x.w, wgt, acc[4 * v + 3]);
+        }
+    }
+    const float inv = 1.f / ll;
+    uint4 *d4 = reinterpret_cast<uint4 *>(p.out + (int64_t(first.q0 + first.m0[a] + r) * p.num_heads + first.h[a]) * D);
+#pragma unroll
+    for (int v = 0; v < D / 8; ++v) {
+        uint4 u;
+        u.x = pa::pack_bf16x2(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv);
+        u.y = pa::pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
+        u.z = pa::pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv);
+        u.w = pa::pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
+        d4[v] = u;
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static std::once_flag once;
@@ -747,6 +846,44 @@ bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int heads, 
 
 int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
 
+// How many key ranges each item is split into: 1 when the call has enough
+// items to fill the GPU twice over, otherwise enough splits to do so, each of
+// at least SPLIT_MIN_TILES K/V tiles (a unit's fill and drain cost several
+// tiles' worth of time, so shorter shares do not pay).
+constexpr int SPLIT_MIN_TILES = 6;
+
+struct PrefillPlan {
+    int n_mtiles, n_steps, units, pair_heads, kv_splits;
+    int64_t items;  // before the key split
+};
+
+PrefillPlan make_prefill_plan(int num_seqs, int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads)
+{
+    PrefillPlan pl;
+    pl.n_mtiles = (max_seqlen_q + BM - 1) / BM;
+    pl.pair_heads = num_heads / num_kv_heads >= 2 ? 1 : 0;
+    pl.n_steps = pl.pair_heads ? pl.n_mtiles : (pl.n_mtiles + 1) / 2;
+    pl.units = pl.pair_heads ? num_heads / 2 : num_heads;
+    pl.items = int64_t(pl.n_steps) * pl.units * num_seqs;
+    pl.kv_splits = 1;
+    const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
+    const int64_t want = 2LL * sms;
+    const int kv_tiles = (max_seqlen_k + BN - 1) / BN;
+    if (pl.items > 0 && pl.items < want && kv_tiles >= 2 * SPLIT_MIN_TILES) {
+        const int64_t by_count = (want + pl.items - 1) / pl.items;
+        const int64_t by_len = kv_tiles / SPLIT_MIN_TILES;
+        pl.kv_splits = int(std::min<int64_t>(std::min<int64_t>(by_count, by_len), 64));
+    }
+    return pl;
+}
+
+size_t prefill_workspace(const PrefillPlan &pl)
+{
+    if (pl.kv_splits <= 1) return 0;
+    const size_t rows = size_t(pl.items) * pl.kv_splits * QT * BM;
+    return (rows * D * sizeof(float) + 255) / 256 * 256 + rows * sizeof(float2);
+}
+
 }  // namespace
 
 extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64_t num_tokens, const void *k,
@@ -756,7 +893,8 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
                                       int max_blocks_per_seq, const int32_t *cu_seqlens_q,
                                       const int32_t *cu_seqlens_k, int num_seqs, int max_seqlen_q,
                                       int max_seqlen_k, int num_heads, int num_kv_heads, int head_dim,
-                                      float scale, void *out, int32_t *dev_status, void *stream)
+                                      float scale, void *out, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, void *stream)
 {
     if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_blocks < 0 || num_tokens < 0)
         return PA_ERR_INVALID_ARG;
@@ -781,7 +919,11 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
         if (!pa::aligned(k_cache, 16) || !pa::aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
         if (num_blocks * block_size >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
     }
-    if (int64_t((max_seqlen_q + BM - 1) / BM) * num_heads * num_seqs > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+    const PrefillPlan pl = make_prefill_plan(num_seqs, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads);
+    if (pl.items * pl.kv_splits > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+    const size_t need = prefill_workspace(pl);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !pa::aligned(workspace, 256)))
+        return PA_ERR_INVALID_ARG;
 
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -794,10 +936,18 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.max_q = max_seqlen_q;
-    p.n_mtiles = (max_seqlen_q + BM - 1) / BM;
-    p.pair_heads = num_heads / num_kv_heads >= 2 ? 1 : 0;
-    p.n_steps = p.pair_heads ? p.n_mtiles : (p.n_mtiles + 1) / 2;
-    p.units = p.pair_heads ? num_heads / 2 : num_heads;
+    p.n_mtiles = pl.n_mtiles;
+    p.pair_heads = pl.pair_heads;
+    p.n_steps = pl.n_steps;
+    p.units = pl.units;
+    p.kv_splits = pl.kv_splits;
+    {
+        const size_t rows = size_t(pl.items) * pl.kv_splits * QT * BM;
+        p.ws_o = need > 0 ? static_cast<float *>(workspace) : nullptr;
+        p.ws_ml = need > 0 ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                                       (rows * D * sizeof(float) + 255) / 256 * 256)
+                           : nullptr;
+    }
     p.num_heads = num_heads;
     p.num_seqs = num_seqs;
     p.kv_heads = num_kv_heads;
@@ -820,12 +970,30 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    const int64_t items = int64_t(p.n_steps) * p.units * num_seqs;
+    const int64_t units = pl.items * pl.kv_splits;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
-    const dim3 grid(unsigned(items < sms ? items : sms));
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(p);
+    const dim3 grid(unsigned(units < sms ? units : sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.kv_splits > 1)
+        prefill_tc_kernel<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    else
+        prefill_tc_kernel<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    if (pl.kv_splits > 1) prefill_merge_kernel<<<dim3(unsigned(pl.items), QT), BM, 0, s>>>(p);
     return pa::launch_status();
+}
+
+extern "C" size_t pa_prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                                             int num_kv_heads)
+{
+    if (num_seqs <= 0 || max_seqlen_q <= 0 || max_seqlen_k < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0)
+        return 0;
+    return prefill_workspace(make_prefill_plan(num_seqs, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads));
 }

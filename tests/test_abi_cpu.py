@@ -83,7 +83,7 @@ def test_prefill_host_checks(lib):
     def call(q=FAKE, qs=2048, nt=16, k=None, v=None, kvs=0, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2,
              cuq=FAKE, cuk=FAKE, ns=2, mq=8, mk=8, hq=16, hkv=8, d=128, out=FAKE):
         return f(q, qs, nt, k, v, kvs, kc, vc, nb, bs, bt, mb, cuq, cuk, ns, mq, mk, hq, hkv, d,
-                 ctypes.c_float(0.1), out, None, None)
+                 ctypes.c_float(0.1), out, None, 0, None, None)
 
     assert call(d=64) == 2
     assert call(hq=12, hkv=8) == 2
