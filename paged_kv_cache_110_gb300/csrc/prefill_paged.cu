@@ -83,7 +83,8 @@ enum {
     B_VE = B_VF + VSTAGES,       // V stage free (every P.V reading it done)
     B_SF = B_VE + VSTAGES,       // S of query tile a computed, per a
     B_PF = B_SF + QT,            // P of query tile a written over its S (128 arrivals), per a
-    B_OF = B_PF + QT,            // O of query tile a complete for the item, per a
+    B_PL = B_PF + QT,            // its first half (keys 0-63) written (128 arrivals), per a
+    B_OF = B_PL + QT,            // O of query tile a complete for the item, per a
     B_TF = B_OF + QT,            // block-id buffer staged (32 arrivals)
     B_TE = B_TF + 2,             // block-id buffer free (both producers done, 2 arrivals)
     B_IRF = B_TE + 2,            // item-ring slot published (1 arrival)
@@ -91,7 +92,7 @@ enum {
     B_DRAIN = B_IRE + RING,
     NBAR = B_DRAIN + 1
 };
-constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA thread, softmax warps
+constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA warp, softmax warps
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag
 constexpr int OFF_RING = OFF_MISC + 16;           // the item ring (RingSlot x RING)
 constexpr int RING_SLOT_BYTES = 96;
@@ -129,6 +130,7 @@ struct TcParams {
     int kv_heads;
     float scale_log2;
     uint16_t *out;
+    int out_v8;       // out is 32-byte aligned: the epilogue stores 32 bytes per instruction
     int32_t *status;
     unsigned int sched_slot;  // which scheduler counter pair this call uses
     int kv_splits;            // key ranges per item (1: no split); split items write partials
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         for (int a = 0; a < QT; ++a) {
             mbar_init(bar(B_SF + a), 1);
             mbar_init(bar(B_PF + a), 128);
+            mbar_init(bar(B_PL + a), 128);
             mbar_init(bar(B_OF + a), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -353,10 +356,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     // the softmax warpgroups hold a 64-column slice of S, its P and O rows in
     // registers; the scheduler, producer and MMA warps need few
     static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= 168 * NTHREADS, "register split");
-    if (warp < 4)
-        regs_decrease<REGS_CONTROL>();
-    else
-        regs_increase<REGS_SOFTMAX>();
+    // (the softmax warpgroups raise theirs at the start of their role below, so
+    // that their code is compiled against the raised budget)
+    if (warp < 4) regs_decrease<REGS_CONTROL>();
 
     // Read item n from the ring (every lane of the calling warp waits; lane 0
     // releases the slot).  Returns the item number, -1 at the end, -2 on abort.
@@ -494,104 +496,120 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // Issue blocks while the tensor pipe is busy, so the issue order below is
         // the execution order: per K/V tile j, P_0.V_j, S_0 of tile j+1, P_1.V_j,
         // S_1 of tile j+1.  The softmax of one query tile thus runs while the
-        // tensor cores work on the other.  One thread runs this role; the
-        // warp's other lanes wait at the end.
-        if (lane == 0) {
-            // shared-memory descriptors of the first Q, K and V buffers; a buffer or
-            // k-step further on adds its byte offset / 16 (the 14-bit address field
-            // cannot overflow below 256 KB)
-            const uint64_t desc_q = smem_desc(sb + OFF_Q, 16, 1024);
-            const uint64_t desc_k = smem_desc(sb + OFF_K, 16, 1024);
-            const uint64_t desc_v = smem_desc(sb + OFF_V, HALF_BYTES, 1024);
-            int t = 0;               // K/V tiles consumed
-            int c[QT] = {0, 0};      // S / P tiles per query tile
-            bool ok = true;
-            for (int n = 0; ok; ++n) {
-                const int slot = n % RING;
-                if (!mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT)) break;
-                const int w = ring[slot].w;
-                if (w < 0) break;
-                const Item it = ring[slot].it;
-                mbar_arrive(bar(B_IRE + slot));
-                {
-                    constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
-                    constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
-                    auto wait = [&](int b, uint32_t parity) {
-                        ok = ok && mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT);
-                        return ok;
-                    };
-                    auto issue_s = [&](int a, int qs, int kst) {
-                        const uint64_t qd = desc_q + uint64_t((qs * TILE_BYTES) >> 4);
-                        const uint64_t kd = desc_k + uint64_t((kst * TILE_BYTES) >> 4);
-                        const uint32_t dst = tmem + 128u * a;
-    #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t off = uint64_t(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
-                            mma_ss(dst, qd + off, kd + off, IDESC_QK, kk > 0);
-                        }
-                        mma_commit(bar(B_SF + a));
-                    };
-                    // first S of each query tile: its S columns still hold P of the
-                    // previous item, whose P.V was issued before (tcgen05 runs in order)
-                    if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
-                        tc_fence_after();
-                        for (int a = 0; a < QT; ++a) {
-                            const int qn = 2 * n + a, qs = qn % QSLOTS;
-                            if (it.nt[a] == 0) {
-                                mma_commit(bar(B_QE + qs));
-                                continue;
-                            }
-                            if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
-                            tc_fence_after();
-                            issue_s(a, qs, t % KSTAGES);
-                            if (it.nt[a] == 1) mma_commit(bar(B_QE + qs));  // the tile's last S
-                        }
-                        if (ok) mma_commit(bar(B_KE + t % KSTAGES));
-                    }
-                    for (int j = 0; ok && j < it.nmax; ++j) {
-                        const int tv = t + j;
-                        bool v_in = false, k_in = false;
-                        for (int a = 0; a < QT; ++a) {
-                            if (j >= it.nt[a]) continue;
-                            if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
-                            if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
-                            tc_fence_after();
-                            const uint64_t vd = desc_v + uint64_t(((tv % VSTAGES) * TILE_BYTES) >> 4);
-                            const uint32_t dst = tmem + COL_O + 128u * a, src = tmem + 128u * a;
-                            const uint32_t acc0 = j > 0 ? 1u : 0u;
-    #pragma unroll
-                            for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(dst, src + kk * 8, vd + uint64_t((kk * 2048) >> 4), IDESC_PV, kk > 0 ? 1u : acc0);
-                            ++c[a];
-                            if (j + 1 < it.nt[a]) {
-                                if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
-                                tc_fence_after();
-                                const int qs = (2 * n + a) % QSLOTS;
-                                issue_s(a, qs, (tv + 1) % KSTAGES);
-                                if (j + 2 == it.nt[a]) mma_commit(bar(B_QE + qs));  // the tile's last S
-                            }
-                        }
-                        if (!ok) break;
-                        mma_commit(bar(B_VE + tv % VSTAGES));
-                        if (j + 1 < it.nmax) mma_commit(bar(B_KE + (tv + 1) % KSTAGES));
-                    }
-                    if (ok) {
-                        for (int a = 0; a < QT; ++a)
-                            if (it.nt[a] > 0) mma_commit(bar(B_OF + a));
-                    }
-                    t += it.nmax;
+        // tensor cores work on the other.  The whole warp runs this loop (every
+        // decision is warp-uniform) and one elected lane issues each tcgen05
+        // instruction: issued that way an MMA costs the issuer a fraction of the
+        // cycles it costs from a lone lane, which would leave the pipe idle.
+        // shared-memory descriptors of the first Q, K and V buffers; a buffer or
+        // k-step further on adds its byte offset / 16 (the 14-bit address field
+        // cannot overflow below 256 KB)
+        const uint64_t desc_q = smem_desc(sb + OFF_Q, 16, 1024);
+        const uint64_t desc_k = smem_desc(sb + OFF_K, 16, 1024);
+        const uint64_t desc_v = smem_desc(sb + OFF_V, HALF_BYTES, 1024);
+        int t = 0;               // K/V tiles consumed
+        int c[QT] = {0, 0};      // S / P tiles per query tile
+        bool ok = true;
+        auto commit = [&](int b) {
+            if (elect_one()) mma_commit(bar(b));
+            __syncwarp();
+        };
+        for (int n = 0; ok; ++n) {
+            const int slot = n % RING;
+            if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) break;
+            const int w = ring[slot].w;
+            if (w < 0) break;
+            const Item it = ring[slot].it;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_IRE + slot));
+            constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
+            constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
+            auto wait = [&](int b, uint32_t parity) {
+                ok = ok && __all_sync(FULL, mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT));
+                return ok;
+            };
+            auto issue_s = [&](int a, int qs, int kst) {
+                const uint64_t qd = desc_q + uint64_t((qs * TILE_BYTES) >> 4);
+                const uint64_t kd = desc_k + uint64_t((kst * TILE_BYTES) >> 4);
+                const uint32_t dst = tmem + 128u * a;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = uint64_t(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+                    if (elect_one()) mma_ss(dst, qd + off, kd + off, IDESC_QK, kk > 0);
                 }
+                __syncwarp();
+                commit(B_SF + a);
+            };
+            // first S of each query tile: its S columns still hold P of the
+            // previous item, whose P.V was issued before (tcgen05 runs in order)
+            if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
+                tc_fence_after();
+                for (int a = 0; a < QT; ++a) {
+                    const int qn = 2 * n + a, qs = qn % QSLOTS;
+                    if (it.nt[a] == 0) {
+                        commit(B_QE + qs);
+                        continue;
+                    }
+                    if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
+                    tc_fence_after();
+                    issue_s(a, qs, t % KSTAGES);
+                    if (it.nt[a] == 1) commit(B_QE + qs);  // the tile's last S
+                }
+                if (ok) commit(B_KE + t % KSTAGES);
             }
-            if (*abort_flag) {
-                // wait for the MMAs already issued before TMEM and shared memory are released
-                volatile int32_t dummy = 0;
-                mma_commit(bar(B_DRAIN));
-                mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
+            for (int j = 0; ok && j < it.nmax; ++j) {
+                const int tv = t + j;
+                bool v_in = false, k_in = false;
+                for (int a = 0; a < QT; ++a) {
+                    if (j >= it.nt[a]) continue;
+                    // P.V in two halves of the keys: the first runs while the
+                    // softmax still computes the second half of P
+                    if (!wait(B_PL + a, uint32_t(c[a]) & 1u)) break;
+                    if (!v_in && !(v_in = wait(B_VF + tv % VSTAGES, par(tv, VSTAGES)))) break;
+                    tc_fence_after();
+                    const uint64_t vd = desc_v + uint64_t(((tv % VSTAGES) * TILE_BYTES) >> 4);
+                    const uint32_t dst = tmem + COL_O + 128u * a, src = tmem + 128u * a;
+                    const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 32; ++kk)
+                        if (elect_one())
+                            mma_ts(dst, src + kk * 8, vd + uint64_t((kk * 2048) >> 4), IDESC_PV, kk > 0 ? 1u : acc0);
+                    __syncwarp();
+                    if (!wait(B_PF + a, uint32_t(c[a]) & 1u)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = BN / 32; kk < BN / 16; ++kk)
+                        if (elect_one())
+                            mma_ts(dst, src + kk * 8, vd + uint64_t((kk * 2048) >> 4), IDESC_PV, 1u);
+                    __syncwarp();
+                    ++c[a];
+                    if (j + 1 < it.nt[a]) {
+                        if (!k_in && !(k_in = wait(B_KF + (tv + 1) % KSTAGES, par(tv + 1, KSTAGES)))) break;
+                        tc_fence_after();
+                        const int qs = (2 * n + a) % QSLOTS;
+                        issue_s(a, qs, (tv + 1) % KSTAGES);
+                        if (j + 2 == it.nt[a]) commit(B_QE + qs);  // the tile's last S
+                    }
+                }
+                if (!ok) break;
+                commit(B_VE + tv % VSTAGES);
+                if (j + 1 < it.nmax) commit(B_KE + (tv + 1) % KSTAGES);
             }
+            if (ok) {
+                for (int a = 0; a < QT; ++a)
+                    if (it.nt[a] > 0) commit(B_OF + a);
+            }
+            t += it.nmax;
+        }
+        if (*abort_flag) {
+            // wait for the MMAs already issued before TMEM and shared memory are released
+            volatile int32_t dummy = 0;
+            commit(B_DRAIN);
+            mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        regs_increase<REGS_SOFTMAX>();
         const int a = (warp - 4) >> 2;  // the query tile of each item this warpgroup owns
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
@@ -627,62 +645,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 const int j0 = (jb + j) * BN;
                 const bool masked = j0 + BN - 1 > it.offset + it.m0[a];  // the tile crosses some row's causal bound
                 const int limit = last_visible - j0;
-                // pass 1: row max of the raw scores
+                // one pass over the row: its 128 scores are loaded from TMEM once,
+                // the row max taken in registers, then P = 2^(s * scale * log2 e - m)
+                // is formed from the same registers, 64 keys at a time; P (bf16
+                // pairs) goes over the S columns already read
+                uint32_t sr[128];
+                tmem_ld128_sync(scol, sr);
+                if (masked) mask_tail(sr, 0, limit);
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+                for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t sr[64];
-                    tmem_ld64_sync(scol + hf * 64, sr);
-                    if (masked) mask_tail(sr, hf * 64, limit);
+                for (int cc = 16; cc < 128; cc += 16) {
 #pragma unroll
-                    for (int cc = 0; cc < 64; cc += 16) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            mx8[k] = fmax3(mx8[k], __uint_as_float(sr[cc + k]), __uint_as_float(sr[cc + 8 + k]));
-                    }
+                    for (int k = 0; k < 8; ++k)
+                        mx8[k] = fmax3(mx8[k], __uint_as_float(sr[cc + k]), __uint_as_float(sr[cc + 8 + k]));
                 }
                 const float mx =
                     fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
                 const bool need = mx > m_used + RESCALE_THRESHOLD;
                 const float m_new = need ? mx : m_used;
                 const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
-                if (j > 0 && __any_sync(FULL, need)) {
-                    // O holds the previous tile's P.V: that P.V was issued before this
-                    // tile's S, whose completion the S barrier reports
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32_sync(ocol + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-                        tmem_st32_sync(ocol + cc * 32, o);
-                    }
-                }
+                const bool rescale_o = j > 0 && __any_sync(FULL, need);
                 l *= factor;
                 m_used = m_new;
                 const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
-                // pass 2: p = 2^(s * scale * log2 e - m), 64 keys at a time; P (bf16
-                // pairs) goes over the S columns already read
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t sr[64];
-                    tmem_ld64_sync(scol + hf * 64, sr);
-                    if (masked) mask_tail(sr, hf * 64, limit);
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x0, x1;
-                        ffma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), sl2, sl2, nm, nm);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        fadd2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
-                        pk[i] = pa::pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32_sync(scol + hf * 32, pk);
-                }
-                l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+                // (before the first half of P is released: P.V of keys 0-63 may read them)
                 if (zeroer && j == it.nmax - 1) {
                     const int tv = tbase + j, sv = tv % VSTAGES;
                     ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), par(tv, VSTAGES), abort_flag, WAIT_LIMIT));
@@ -695,6 +683,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     }
                     fence_proxy_async_smem();
                 }
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x0, x1;
+                        ffma2(x0, x1, __uint_as_float(sr[64 * hf + 2 * i]), __uint_as_float(sr[64 * hf + 2 * i + 1]), sl2,
+                              sl2, nm, nm);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        fadd2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
+                        pk[i] = pa::pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32_sync(scol + hf * 32, pk);
+                    if (hf == 0) {
+                        if (rescale_o) {
+                            // O holds the previous tile's P.V: that P.V was issued before
+                            // this tile's S, whose completion the S barrier reported; the
+                            // P.V of this tile starts only after the arrival below
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc) {
+                                uint32_t o[32];
+                                tmem_ld32_sync(ocol + cc * 32, o);
+#pragma unroll
+                                for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
+                                tmem_st32_sync(ocol + cc * 32, o);
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(bar(B_PL + a));
+                    }
+                }
+                l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
                 tc_fence_before();
                 mbar_arrive(bar(B_PF + a));
             }
@@ -714,11 +735,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     uint32_t o[64];
                     tmem_ld64_sync(ocol + hf * 64, o);
                     if (r < it.rows[a]) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + row * D + hf * 64);
+                        float *dst = p.ws_o + row * D + hf * 64;  // 256-byte aligned rows
 #pragma unroll
-                        for (int v = 0; v < 16; ++v)
-                            dst[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                                 __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                        for (int v = 0; v < 8; ++v) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w8[e] = o[8 * v + e];
+                            st_global_v8(dst + 8 * v, w8);
+                        }
                     }
                 }
                 if (r < it.rows[a]) p.ws_ml[row] = make_float2(m_used, l);
@@ -729,7 +753,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t o[64];
                 tmem_ld64_sync(ocol + hf * 64, o);
-                if (r < it.rows[a]) {
+                if (r < it.rows[a] && p.out_v8) {
+                    uint16_t *dst = p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D + hf * 64;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w8[e] = pa::pack_bf16x2(__uint_as_float(o[16 * v + 2 * e]) * inv,
+                                                    __uint_as_float(o[16 * v + 2 * e + 1]) * inv);
+                        st_global_v8(dst + 16 * v, w8);
+                    }
+                } else if (r < it.rows[a]) {
                     uint4 *d4 =
                         reinterpret_cast<uint4 *>(p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D);
 #pragma unroll
@@ -953,6 +988,7 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
     p.kv_heads = num_kv_heads;
     p.scale_log2 = scale * LOG2E;
     p.out = static_cast<uint16_t *>(out);
+    p.out_v8 = pa::aligned(out, 32) ? 1 : 0;
     p.status = dev_status;
     static std::atomic<unsigned> next_slot{0};
     p.sched_slot = next_slot.fetch_add(1u, std::memory_order_relaxed) % SCHED_SLOTS;

@@ -146,6 +146,31 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// One lane of the (converged) warp: the lowest active lane.  tcgen05.mma and
+// tcgen05.commit issued under it from a warp that runs the issue loop together
+// cost far fewer cycles per instruction than the same instructions issued from
+// a lone lane while the other lanes wait at a branch.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// 32-byte store to global memory (sm_100 and later); the address must be
+// 32-byte aligned.  A warp of these at a large stride still writes whole
+// 32-byte sectors, where 16-byte stores would write half sectors.
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate)

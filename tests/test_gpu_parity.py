@@ -95,6 +95,24 @@ def test_prefill_varlen_16k():
     _prefill_case(wl.varlen_prefill(device=dev()))
 
 
+@pytest.mark.parametrize("growth", [0.02, 0.002], ids=["jump_every_tile", "slow_growth"])
+@pytest.mark.parametrize("lens", [[700, 1024, 129, 300], [1600]], ids=["batch", "one_long_split"])
+def test_prefill_growing_scores_rescale(growth, lens):
+    """Scores that grow along the key positions: with q >= 0 and every key
+    equal to growth * position, a later key tile's scores exceed the running
+    maximum by about 33 (growth 0.02) or 3 (growth 0.002) in log2 units per
+    128 keys, so the online softmax moves its maximum and rescales O on nearly
+    every tile, inside masked diagonal tiles too, or runs on a stale maximum
+    for several tiles.  The single long sequence is a small call whose keys
+    are split across CTAs and merged."""
+    lens = np.array(lens, dtype=np.int32)
+    batch = wl.paged_batch(wl.SEED_BASE + 41, lens, lens, 64, device=dev())
+    pos = torch.as_tensor(batch.positions, device=dev(), dtype=torch.float32)
+    batch.tokens.q.copy_(batch.tokens.q.abs())
+    batch.tokens.k.copy_((growth * pos)[:, None, None].expand_as(batch.tokens.k).to(torch.bfloat16))
+    _prefill_case(batch)
+
+
 @pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 16), (8, 8, 32), (8, 1, 64), (32, 4, 128), (4, 2, 256),
                                        (2, 2, 48)])
 def test_prefill_shapes_with_cached_prefix(hq, hkv, bs):
