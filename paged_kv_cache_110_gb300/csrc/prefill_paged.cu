@@ -18,7 +18,7 @@
 // (S -> softmax -> P.V) hide each other.
 //   warp 3      scheduler: fetches items, decodes each once and publishes it
 //               in a ring of 4, stages its block ids (validated) and loads its
-//               two Q tiles by TMA into a ring of three Q buffers.
+//               two Q tiles by TMA into two Q buffers.
 //   warp 0      K producer, warp 2 V producer: paged tiles arrive by TMA, one
 //               box per page run (box height gcd(block_size, 128) rows, so a
 //               box never crosses a page); without a table one box of 128
@@ -28,14 +28,16 @@
 //               sequence's rows, TMA zero fill, unused pool slots) are masked
 //               out of S, and the V rows of the item's last tile past its last
 //               key are set to zero before P.V, so that they add 0.
-//   warp 1      MMA issuer (one thread): per K/V tile j, O_0 += P_0 V_j then
-//               S_0 = Q_0 K_{j+1}^T, then the same for query tile 1.  S and O of
-//               each query tile live in TMEM (S at columns 0 / 128, O at
-//               256 / 384); P is written back over S, and the next S is issued
-//               after the P.V that reads P (tcgen05 operations run in order).
+//   warp 1      MMA issuer (the warp runs the loop, one elected lane issues):
+//               per K/V tile j, O_0 += P_0 V_j (keys 0-63 as soon as their P is
+//               written, then 64-127) then S_0 = Q_0 K_{j+1}^T, then the same
+//               for query tile 1.  S and O of each query tile live in TMEM (S
+//               at columns 0 / 128, O at 256 / 384); P is written back over S,
+//               and the next S is issued after the P.V that reads P (tcgen05
+//               operations run in order).
 //   warps 4-7, 8-11   softmax of query tile 0 and 1, one thread per row: read
-//               the S row from TMEM, mask (causal, bottom-right, keys past the
-//               last visible key), row max, base-2 exponentials with
+//               the S row from TMEM once, mask (causal, bottom-right, keys past
+//               the last visible key), row max, base-2 exponentials with
 //               scale * log2(e) folded into paired FMAs, row sums, P as bf16
 //               over S.  The running max is raised only when a row max grows
 //               by more than 8 (a factor 256), and only then is the O row
@@ -63,7 +65,7 @@ constexpr int QT = 2;               // query tiles per work item, sharing every 
 constexpr int BN = 128;             // keys per tile
 constexpr int KSTAGES = 2;          // K tiles in flight
 constexpr int VSTAGES = 2;          // V tiles in flight
-constexpr int QSLOTS = 3;           // Q tile buffers: one item's pair and the next item's first tile
+constexpr int QSLOTS = 2;           // Q tile buffers: one item's pair
 constexpr int RING = 4;             // work items fetched ahead by the scheduler warp
 constexpr int NTHREADS = 384;
 constexpr uint32_t REGS_CONTROL = 136;  // per thread, warps 0-3 (one warpgroup)
