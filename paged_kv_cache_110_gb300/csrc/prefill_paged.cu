@@ -803,11 +803,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
 // Combine the key-range shares of every split item: per query row,
 // M = max_s m_s, L = sum_s l_s 2^(m_s - M), out = sum_s O_s 2^(m_s - M) / L
-// ("大模型推理入门与 nano-vLLM 源码详解" §9.5).  A CTA per (item, query tile), a
-// thread per row.
-__global__ void __launch_bounds__(BM) prefill_merge_kernel(const __grid_constant__ TcParams p)
+// ("大模型推理入门与 nano-vLLM 源码详解" §9.5).  A CTA per (item, query tile, 16
+// rows); 16 threads per row, 8 columns each, so that a row's 512-byte shares
+// are read by contiguous threads.
+constexpr int MERGE_ROWS = 16;
+__global__ void __launch_bounds__(MERGE_ROWS * 16) prefill_merge_kernel(const __grid_constant__ TcParams p)
 {
-    const int a = blockIdx.y, r = threadIdx.x;
+    const int a = blockIdx.y;
+    const int r = blockIdx.z * MERGE_ROWS + int(threadIdx.x >> 4);
+    const int c8 = int(threadIdx.x & 15) * 8;  // this thread's first column
     const int w0 = blockIdx.x * p.kv_splits;
     const Item first = decode_item<true>(p, w0);
     if (!first.split || first.bad || r >= first.rows[a]) return;
@@ -816,9 +820,7 @@ __global__ void __launch_bounds__(BM) prefill_merge_kernel(const __grid_constant
         const Item it = decode_item<true>(p, w0 + s);
         if (it.valid && it.nt[a] > 0) mm = fmaxf(mm, p.ws_ml[(int64_t(w0 + s) * QT + a) * BM + r].x);
     }
-    float acc[D];
-#pragma unroll
-    for (int e = 0; e < D; ++e) acc[e] = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float ll = 0.f;
     for (int s = 0; s < p.kv_splits; ++s) {
         const Item it = decode_item<true>(p, w0 + s);
@@ -827,27 +829,24 @@ __global__ void __launch_bounds__(BM) prefill_merge_kernel(const __grid_constant
         const float2 ml = p.ws_ml[row];
         const float wgt = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - mm);
         ll = fmaf(ml.y, wgt, ll);
-        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * D);
-#pragma unroll
-        for (int v = 0; v < D / 4; ++v) {
-            const float4 x = src[v];
-            acc[4 * v] = fmaf(x.x, wgt, acc[4 * v]);
-            acc[4 * v + 1] = fmaf(x.y, wgt, acc[4 * v + 1]);
-            acc[4 * v + 2] = fmaf(x.z, wgt, acc[4 * v + 2]);
-            acc[4 * v + 3] = fmaf(x.w, wgt, acc[4 * v + 3]);
-        }
+        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * D + c8);
+        const float4 x0 = src[0], x1 = src[1];
+        acc[0] = fmaf(x0.x, wgt, acc[0]);
+        acc[1] = fmaf(x0.y, wgt, acc[1]);
+        acc[2] = fmaf(x0.z, wgt, acc[2]);
+        acc[3] = fmaf(x0.w, wgt, acc[3]);
+        acc[4] = fmaf(x1.x, wgt, acc[4]);
+        acc[5] = fmaf(x1.y, wgt, acc[5]);
+        acc[6] = fmaf(x1.z, wgt, acc[6]);
+        acc[7] = fmaf(x1.w, wgt, acc[7]);
     }
     const float inv = 1.f / ll;
-    uint4 *d4 = reinterpret_cast<uint4 *>(p.out + (int64_t(first.q0 + first.m0[a] + r) * p.num_heads + first.h[a]) * D);
-#pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-        uint4 u;
-        u.x = pa::pack_bf16x2(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv);
-        u.y = pa::pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
-        u.z = pa::pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv);
-        u.w = pa::pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
-        d4[v] = u;
-    }
+    uint4 u;
+    u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(p.out + (int64_t(first.q0 + first.m0[a] + r) * p.num_heads + first.h[a]) * D + c8) = u;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -1023,7 +1022,8 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
         prefill_tc_kernel<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
     else
         prefill_tc_kernel<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
-    if (pl.kv_splits > 1) prefill_merge_kernel<<<dim3(unsigned(pl.items), QT), BM, 0, s>>>(p);
+    if (pl.kv_splits > 1)
+        prefill_merge_kernel<<<dim3(unsigned(pl.items), QT, BM / MERGE_ROWS), MERGE_ROWS * 16, 0, s>>>(p);
     return pa::launch_status();
 }
 
