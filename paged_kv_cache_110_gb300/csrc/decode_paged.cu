@@ -196,6 +196,9 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     const int b = blockIdx.x, s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, c = lane & 15;
+    // launched programmatically: everything below may depend on the previous
+    // kernel (the KV write of this step's token)
+    pa::grid_dependency_wait();
 
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) {
@@ -341,6 +344,9 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
     }
 
+    // this CTA's loads are done: the next kernel (the merge) may start launching
+    pa::grid_dependents_launch();
+
     // the two halves saw different tokens of the same chunks: add them
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -416,6 +422,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 {
+    pa::grid_dependency_wait();  // the split kernel's partials
+    pa::grid_dependents_launch();
     const int b = blockIdx.x;
     int ctx = p.context_lens[b];
     if (ctx <= 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) return;
@@ -476,7 +484,7 @@ template <int G, bool FP8>
 void launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
-    decode_split_kernel<G, FP8><<<grid, NW * 32, 0, stream>>>(p);
+    pa::launch_pdl(decode_split_kernel<G, FP8>, grid, dim3(NW * 32), 0, stream, p);
 }
 
 pa_status check_args(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
@@ -567,7 +575,7 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
         default: launch_split<8, false>(p, s); break;
         }
     }
-    if (plan.max_splits > 1) decode_merge_kernel<<<dim3(unsigned(num_seqs)), 256, 0, s>>>(p);
+    if (plan.max_splits > 1) pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs)), dim3(256), 0, s, p);
     return pa::launch_status();
 }
 

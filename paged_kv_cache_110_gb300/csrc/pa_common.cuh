@@ -37,6 +37,35 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the kernel before it in the stream is still finishing; it must call
+// grid_dependency_wait() before it reads or writes anything that kernel (or
+// any earlier work) may touch: the wait returns once the earlier grid has
+// completed and its memory operations are visible.  Without a programmatic
+// predecessor the wait returns at once.  grid_dependents_launch() lets the
+// NEXT kernel start early (once every CTA of this one has called it or
+// exited); its CTAs then occupy SM slots while they wait, so a long kernel
+// calls it only near its end.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 inline bool aligned(const void *p, size_t bytes)
 {
     return (reinterpret_cast<uintptr_t>(p) % bytes) == 0;

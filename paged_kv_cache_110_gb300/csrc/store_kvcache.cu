@@ -47,6 +47,10 @@ store_kvcache_kernel(const char *__restrict__ k, int64_t k_stride_bytes,
                      const int32_t *__restrict__ slot_mapping, int32_t *status)
 {
     using T = typename Vec<VEC>::T;
+    // launched programmatically: the previous kernel's writes (a decode that
+    // read the pool, the projection that wrote k / v) are complete only after this
+    pa::grid_dependency_wait();
+    pa::grid_dependents_launch();  // a short kernel: the next one may launch now
     const int64_t per_token = int64_t(2) << log2_vecs;
     const int64_t total = num_tokens * per_token;
     const int64_t step = int64_t(gridDim.x) * blockDim.x;
@@ -79,9 +83,9 @@ void launch(const void *k, int64_t ks, const void *v, int64_t vs, int64_t num_to
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = int64_t(pa::num_sms() > 0 ? pa::num_sms() : 152) * 64;
     if (blocks > cap) blocks = cap;
-    store_kvcache_kernel<VEC><<<dim3(unsigned(blocks)), threads, 0, stream>>>(
-        static_cast<const char *>(k), ks * 2, static_cast<const char *>(v), vs * 2, num_tokens, log2_vecs,
-        static_cast<char *>(kc), static_cast<char *>(vc), num_slots, row_bytes, slots, status);
+    pa::launch_pdl(store_kvcache_kernel<VEC>, dim3(unsigned(blocks)), dim3(threads), 0, stream,
+                   static_cast<const char *>(k), ks * 2, static_cast<const char *>(v), vs * 2, num_tokens, log2_vecs,
+                   static_cast<char *>(kc), static_cast<char *>(vc), num_slots, row_bytes, slots, status);
 }
 
 }  // namespace
