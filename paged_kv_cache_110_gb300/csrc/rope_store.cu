@@ -128,16 +128,18 @@ __global__ void __launch_bounds__(128) norm_rope_store_kernel(const RopeParams p
         const int64_t t = u / units_per_token;
         const int r0 = int(u - t * units_per_token) * 2 * CHUNK;
         const int64_t pos = p.positions[t], slot = p.slots[t];
-        if (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots))) {
-            if (lane == 0 && r0 == 0) pa::report(p.status, PA_ERR_BOUNDS);
-            continue;  // the whole warp skips the unit
-        }
+        // the rows do not depend on the position: their loads go out before the
+        // position is back and checked, so the two waits overlap
         const uint16_t *src = p.qkv + t * p.qkv_stride + sub * 8;
         uint4 raw[CHUNK];
 #pragma unroll
         for (int k = 0; k < CHUNK; ++k) {
             const int r = r0 + 2 * k + hw;
             raw[k] = r < rows ? *reinterpret_cast<const uint4 *>(src + int64_t(r) * D) : make_uint4(0, 0, 0, 0);
+        }
+        if (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots))) {
+            if (lane == 0 && r0 == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            continue;  // the whole warp skips the unit
         }
         const float *cs = p.cos_sin + pos * D + (sub & 7) * 8;
         float c[8], s[8];
