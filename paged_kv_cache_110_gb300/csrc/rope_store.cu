@@ -15,14 +15,16 @@
 //     slot_mapping[t] (slot -1: nothing is stored).
 //
 // Design: bound by HBM (per token at Hq = 16, Hkv = 8: 8 KiB of QKV read, 4 KiB
-// of Q and 4 KiB of K/V written, 512 B of table read through L1/L2).  A warp
-// owns 16 head rows of a token: it reads the token's position, slot and
-// table row, then the rows two at a time, a half-warp per 256-byte row (16
-// lanes x 8 features, one 16-byte load and store each), eight rows per
-// half-warp loaded before any is used so that many loads are in flight.  The sum of squares is
+// of Q and 4 KiB of K/V written, 512 B of table read through L2).  A producer
+// warp streams whole token rows into shared memory with bulk copies, several
+// tokens ahead; the compute warps take a 256-byte head row per half-warp (16
+// lanes x 8 features, one 16-byte store each).  The sum of squares is
 // reduced over the half-warp, and the RoPE partner of lane l's features is
 // lane l ^ 8.
+#include <mutex>
+
 #include "pa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -107,66 +109,138 @@ __device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint4 *w, float eps
     return pack8(out);
 }
 
-constexpr int CHUNK = 8;  // rows per half-warp whose loads are issued together
+// Work: one token at a time per CTA (tokens blockIdx.x, + gridDim.x, ...).
+// Warp 4 streams each token's whole QKV row (rows x 256 B, contiguous) and its
+// cos / sin row into a ring of STAGES shared-memory stages with bulk copies,
+// several tokens ahead, so the bytes in flight do not depend on registers;
+// warps 0-3 take the rows of the token in the front stage, a half-warp per
+// 256-byte row, and write Q, K and V out with 16-byte stores.
+constexpr int STAGES = 4;
+constexpr int COMPUTE_WARPS = 4;
+constexpr int RS_THREADS = (COMPUTE_WARPS + 1) * 32;
+constexpr long long RS_WAIT_LIMIT = 1ll << 31;  // SM cycles (about a second)
 
-// Work unit: 2 * CHUNK consecutive head rows (Q heads, K heads, V heads) of
-// one token, a warp per unit (grid-stride).  The token's position, slot and
-// table row are read per unit (the second unit of a token finds them in L1);
-// the half-warps take alternate rows, CHUNK rows each, all loaded before any
-// is used.
-__global__ void __launch_bounds__(128) norm_rope_store_kernel(const RopeParams p)
+struct StageInfo {
+    int32_t pos, slot, ok, pad;
+};
+
+// Bytes of one stage: the QKV row, the 512-byte cos / sin row, the info,
+// rounded to 128 bytes.
+__host__ __device__ inline int stage_bytes(int rows) { return (rows * D * 2 + 2 * HALF * 4 + 16 + 127) / 128 * 128; }
+
+__global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeParams p)
 {
-    const int lane = threadIdx.x & 31, sub = lane & 15, hw = lane >> 4;
+    extern __shared__ __align__(128) uint8_t sm[];
+    using namespace pa::sm100;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane & 15, hw = lane >> 4;
     const int rows = p.num_heads + 2 * p.kv_heads;
-    const int units_per_token = (rows + 2 * CHUNK - 1) / (2 * CHUNK);
-    const int64_t units = p.num_tokens * units_per_token;
-    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-    uint4 wq = make_uint4(0, 0, 0, 0), wk = wq;
-    if (p.q_weight) wq = *reinterpret_cast<const uint4 *>(p.q_weight + sub * 8);
-    if (p.k_weight) wk = *reinterpret_cast<const uint4 *>(p.k_weight + sub * 8);
-    for (int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < units; u += warps) {
-        const int64_t t = u / units_per_token;
-        const int r0 = int(u - t * units_per_token) * 2 * CHUNK;
-        const int64_t pos = p.positions[t], slot = p.slots[t];
-        // the rows do not depend on the position: their loads go out before the
-        // position is back and checked, so the two waits overlap
-        const uint16_t *src = p.qkv + t * p.qkv_stride + sub * 8;
-        uint4 raw[CHUNK];
-#pragma unroll
-        for (int k = 0; k < CHUNK; ++k) {
-            const int r = r0 + 2 * k + hw;
-            raw[k] = r < rows ? *reinterpret_cast<const uint4 *>(src + int64_t(r) * D) : make_uint4(0, 0, 0, 0);
+    const uint32_t row_bytes = uint32_t(rows) * D * 2;
+    const int sbytes = stage_bytes(rows);
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bars = sbase + STAGES * sbytes;  // full[STAGES], empty[STAGES]
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + STAGES * sbytes + 2 * STAGES * 8);
+    auto full = [&](int s) { return bars + 8u * uint32_t(s); };
+    auto empty = [&](int s) { return bars + 8u * uint32_t(STAGES + s); };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), COMPUTE_WARPS);
         }
-        if (pos < 0 || pos >= p.max_positions || (slot != -1 && (slot < 0 || slot >= p.num_slots))) {
-            if (lane == 0 && r0 == 0) pa::report(p.status, PA_ERR_BOUNDS);
-            continue;  // the whole warp skips the unit
-        }
-        const float *cs = p.cos_sin + pos * D + (sub & 7) * 8;
-        float c[8], s[8];
-        {
-            const float4 c0 = *reinterpret_cast<const float4 *>(cs), c1 = *reinterpret_cast<const float4 *>(cs + 4);
-            const float4 s0 = *reinterpret_cast<const float4 *>(cs + HALF);
-            const float4 s1 = *reinterpret_cast<const float4 *>(cs + HALF + 4);
-            c[0] = c0.x, c[1] = c0.y, c[2] = c0.z, c[3] = c0.w, c[4] = c1.x, c[5] = c1.y, c[6] = c1.z, c[7] = c1.w;
-            s[0] = s0.x, s[1] = s0.y, s[2] = s0.z, s[3] = s0.w, s[4] = s1.x, s[5] = s1.y, s[6] = s1.z, s[7] = s1.w;
-        }
-#pragma unroll
-        for (int k = 0; k < CHUNK; ++k) {
-            const int r = r0 + 2 * k + hw;
-            if (r0 + 2 * k >= rows) break;  // warp-uniform: no row left for either half-warp
-            const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
-            const bool has_w = is_q ? p.q_weight != nullptr : (is_k && p.k_weight != nullptr);
-            const uint4 y = norm_rope8(raw[k], has_w ? (is_q ? &wq : &wk) : nullptr, p.eps, c, s, sub);
-            if (r >= rows) continue;
-            if (is_q) {
-                *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
-            } else if (slot != -1) {
-                const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
-                uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (slot * p.kv_heads + g) * D + sub * 8;
-                *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw[k];
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // launched programmatically: the QKV rows, positions and slots come from
+    // the kernels before this one
+    pa::grid_dependency_wait();
+    const int64_t T = p.num_tokens;
+
+    if (warp == COMPUTE_WARPS) {
+        // ------------------------------------------------ producer
+        // the positions and slots of 32 of this CTA's tokens are read at once
+        // (a lane each), then lane 0 issues their copies one stage at a time
+        int k = 0;
+        bool ok = true;
+        for (int64_t t0 = blockIdx.x; ok && t0 < T; t0 += 32 * int64_t(gridDim.x)) {
+            const int64_t tl = t0 + int64_t(lane) * gridDim.x;
+            int32_t pos = 0, slot = -1;
+            if (tl < T) {
+                pos = p.positions[tl];
+                slot = p.slots[tl];
+            }
+            for (int l = 0; l < 32; ++l, ++k) {
+                const int64_t t = t0 + int64_t(l) * gridDim.x;
+                if (t >= T) break;
+                const int32_t pl = __shfl_sync(FULL, pos, l), sl = __shfl_sync(FULL, slot, l);
+                const int s = k % STAGES;
+                if (k >= STAGES) {
+                    ok = __all_sync(FULL, mbar_wait(empty(s), uint32_t((k - STAGES) / STAGES) & 1u, abort_flag,
+                                                    RS_WAIT_LIMIT));
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    const bool good = pl >= 0 && pl < p.max_positions &&
+                                      (sl == -1 || (sl >= 0 && int64_t(sl) < p.num_slots));
+                    StageInfo *info = reinterpret_cast<StageInfo *>(sm + s * sbytes + row_bytes + 2 * HALF * 4);
+                    *info = StageInfo{pl, sl, good ? 1 : 0, 0};
+                    const uint32_t dst = sbase + uint32_t(s * sbytes);
+                    mbar_arrive_expect_tx(full(s), row_bytes + (good ? 2u * HALF * 4u : 0u));
+                    bulk_load(dst, p.qkv + t * p.qkv_stride, row_bytes, full(s));
+                    if (good) bulk_load(dst + row_bytes, p.cos_sin + int64_t(pl) * D, 2 * HALF * 4, full(s));
+                }
+                __syncwarp();
             }
         }
+        // copies still in flight must land before the CTA's shared memory goes
+        // away: wait (bounded, whatever the abort flag says) for the last ones
+        if (lane == 0) {
+            volatile int32_t dummy = 0;
+            for (int u = max(0, k - STAGES); u < k; ++u)
+                mbar_wait(full(u % STAGES), uint32_t(u / STAGES) & 1u, &dummy, RS_WAIT_LIMIT);
+        }
+    } else {
+        // ------------------------------------------------ compute warps
+        uint4 wq = make_uint4(0, 0, 0, 0), wk = wq;
+        if (p.q_weight) wq = *reinterpret_cast<const uint4 *>(p.q_weight + sub * 8);
+        if (p.k_weight) wk = *reinterpret_cast<const uint4 *>(p.k_weight + sub * 8);
+        const int iters = (rows + 2 * COMPUTE_WARPS - 1) / (2 * COMPUTE_WARPS);
+        int k = 0;
+        for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++k) {
+            const int s = k % STAGES;
+            if (!__all_sync(FULL, mbar_wait(full(s), uint32_t(k / STAGES) & 1u, abort_flag, RS_WAIT_LIMIT))) break;
+            const uint8_t *stage = sm + s * sbytes;
+            const StageInfo info = *reinterpret_cast<const StageInfo *>(stage + row_bytes + 2 * HALF * 4);
+            if (!info.ok) {
+                if (warp == 0 && lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            } else {
+                const float *cs = reinterpret_cast<const float *>(stage + row_bytes) + (sub & 7) * 8;
+                float c[8], sn[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c[i] = cs[i], sn[i] = cs[HALF + i];
+                for (int it = 0; it < iters; ++it) {
+                    const int r = (it * COMPUTE_WARPS + warp) * 2 + hw;
+                    const bool live = r < rows;
+                    const uint4 raw = live ? *reinterpret_cast<const uint4 *>(stage + r * D * 2 + sub * 16)
+                                           : make_uint4(0, 0, 0, 0);
+                    const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
+                    const bool has_w = is_q ? p.q_weight != nullptr : (is_k && p.k_weight != nullptr);
+                    const uint4 y = norm_rope8(raw, has_w ? (is_q ? &wq : &wk) : nullptr, p.eps, c, sn, sub);
+                    if (!live) continue;
+                    if (is_q) {
+                        *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
+                    } else if (info.slot != -1) {
+                        const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
+                        uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (int64_t(info.slot) * p.kv_heads + g) * D +
+                                        sub * 8;
+                        *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
+        }
     }
+    if (threadIdx.x == 0 && *abort_flag) pa::report(p.status, PA_ERR_TIMEOUT);
 }
 
 // Row p of the table: cos(p * f_i) for i < head_dim / 2, then sin(p * f_i),
@@ -248,12 +322,20 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     p.num_slots = num_blocks * block_size;
     p.slots = slot_mapping;
     p.status = dev_status;
-    // a warp per unit of 16 head rows, four warps per block
-    const int64_t units = num_tokens * ((num_heads + 2 * num_kv_heads + 15) / 16);
-    const int64_t blocks = (units + 3) / 4;
+    // a CTA per token at a time, four CTAs per SM
+    const int rows = num_heads + 2 * num_kv_heads;
+    const size_t smem = size_t(STAGES) * stage_bytes(rows) + 2 * STAGES * 8 + 16;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        // the largest QKV row: 64 query heads and 8 KV heads
+        const size_t most = size_t(STAGES) * stage_bytes(64 + 2 * 8) + 2 * STAGES * 8 + 16;
+        attr_err = cudaFuncSetAttribute(norm_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
+    });
+    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
-    const int64_t cap = int64_t(sms) * 16;
-    const unsigned grid = unsigned(blocks < cap ? blocks : cap);
-    norm_rope_store_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    const int64_t cap = int64_t(sms) * 4;
+    const unsigned grid = unsigned(num_tokens < cap ? num_tokens : cap);
+    pa::launch_pdl(norm_rope_store_kernel, dim3(grid), dim3(RS_THREADS), smem, static_cast<cudaStream_t>(stream), p);
     return pa::launch_status();
 }
