@@ -222,6 +222,16 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
                     const bool live = r < rows;
                     const uint4 raw = live ? *reinterpret_cast<const uint4 *>(stage + r * D * 2 + sub * 16)
                                            : make_uint4(0, 0, 0, 0);
+                    if (r - hw >= p.num_heads + p.kv_heads) {
+                        // both rows of the pair are V rows (Hq + Hkv is even, so a pair
+                        // never straddles K and V): copied unchanged, no norm or rotation
+                        if (live && info.slot != -1) {
+                            const int g = r - p.num_heads - p.kv_heads;
+                            *reinterpret_cast<uint4 *>(p.v_cache + (int64_t(info.slot) * p.kv_heads + g) * D +
+                                                       sub * 8) = raw;
+                        }
+                        continue;
+                    }
                     const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
                     const bool has_w = is_q ? p.q_weight != nullptr : (is_k && p.k_weight != nullptr);
                     const uint4 y = norm_rope8(raw, has_w ? (is_q ? &wq : &wk) : nullptr, p.eps, c, sn, sub);
@@ -322,7 +332,8 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     p.num_slots = num_blocks * block_size;
     p.slots = slot_mapping;
     p.status = dev_status;
-    // a CTA per token at a time, four CTAs per SM
+    // a CTA per token at a time, six CTAs per SM (what shared memory allows at
+    // 16 query and 8 KV heads)
     const int rows = num_heads + 2 * num_kv_heads;
     const size_t smem = size_t(STAGES) * stage_bytes(rows) + 2 * STAGES * 8 + 16;
     static std::once_flag once;
@@ -334,7 +345,7 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
-    const int64_t cap = int64_t(sms) * 4;
+    const int64_t cap = int64_t(sms) * 6;
     const unsigned grid = unsigned(num_tokens < cap ? num_tokens : cap);
     pa::launch_pdl(norm_rope_store_kernel, dim3(grid), dim3(RS_THREADS), smem, static_cast<cudaStream_t>(stream), p);
     return pa::launch_status();
