@@ -50,8 +50,6 @@ struct RopeParams {
     int32_t *status;
 };
 
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8])
 {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -82,15 +80,24 @@ __device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint4 *w, float eps
     for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    uint32_t mw[4];  // x as bf16 pairs (exact: x holds bf16 values)
     if (w != nullptr) {
         const float r = 1.0f / sqrtf(ss * (1.0f / D) + eps);
         float wv[8];
         unpack8(*w, wv);
+        // x = bf16(bf16(x * r) * w), two elements per conversion instruction
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = bf16_round(bf16_round(x[i] * r) * wv[i]);
+        for (int i = 0; i < 8; i += 2) {
+            const uint32_t a = pa::pack_bf16x2(x[i] * r, x[i + 1] * r);
+            mw[i / 2] = pa::pack_bf16x2(pa::bf16_lo(a) * wv[i], pa::bf16_hi(a) * wv[i + 1]);
+            x[i] = pa::bf16_lo(mw[i / 2]);
+            x[i + 1] = pa::bf16_hi(mw[i / 2]);
+        }
+    } else {
+        mw[0] = raw.x, mw[1] = raw.y, mw[2] = raw.z, mw[3] = raw.w;
     }
     // partner features (i +- 64) live in lane sub ^ 8
-    const uint4 mine = pack8(x);  // exact: x already holds bf16 values
+    const uint4 mine = make_uint4(mw[0], mw[1], mw[2], mw[3]);
     uint4 other;
     other.x = __shfl_xor_sync(FULL, mine.x, 8);
     other.y = __shfl_xor_sync(FULL, mine.y, 8);
