@@ -17,10 +17,10 @@
 // Design: bound by HBM (per token at Hq = 16, Hkv = 8: 8 KiB of QKV read, 4 KiB
 // of Q and 4 KiB of K/V written, 512 B of table read through L2).  A producer
 // warp streams whole token rows into shared memory with bulk copies, several
-// tokens ahead; the compute warps take a 256-byte head row per half-warp (16
-// lanes x 8 features, one 16-byte store each).  The sum of squares is
-// reduced over the half-warp, and the RoPE partner of lane l's features is
-// lane l ^ 8.
+// tokens ahead; the compute warps take a 256-byte head row per half-warp, lane
+// j holding features 4j .. 4j+3 and their rotation partners 64+4j .. 64+4j+3
+// (two 8-byte pieces), so the rotation needs no exchange between lanes; the
+// sum of squares is reduced over the half-warp.
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -50,70 +50,46 @@ struct RopeParams {
     int32_t *status;
 };
 
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8])
+// Norm (when w != null) and rotate the lane's 4 rotation pairs: lo holds
+// features 4j .. 4j+3 and hi features 64+4j .. 64+4j+3 (j = the lane's index in
+// its half-warp), so a pair (a, b) = (feature i, feature i + 64) sits in one
+// lane; c / s are the cos and sin of those 4 pairs.  Every lane of the warp
+// must call this (the sum of squares is reduced over the half-warp).
+__device__ __forceinline__ void norm_rope_pairs(uint2 &lo, uint2 &hi, const uint2 *wlo, const uint2 *whi, float eps,
+                                                const float (&c)[4], const float (&s)[4])
 {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = pa::bf16_lo(w[i]);
-        x[2 * i + 1] = pa::bf16_hi(w[i]);
-    }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&x)[8])
-{
-    return make_uint4(pa::pack_bf16x2(x[0], x[1]), pa::pack_bf16x2(x[2], x[3]), pa::pack_bf16x2(x[4], x[5]),
-                      pa::pack_bf16x2(x[6], x[7]));
-}
-
-// Norm (when w != null) and rotate the 8 features of this lane; `sub` is the
-// lane's index within its half-warp, c / s the cos and sin of the lane's 8
-// pairs.  Every lane of the warp must call this (it shuffles).
-__device__ __forceinline__ uint4 norm_rope8(uint4 raw, const uint4 *w, float eps, const float (&c)[8],
-                                            const float (&s)[8], int sub)
-{
-    float x[8];
-    unpack8(raw, x);
-    // offsets below 16 stay within a half-warp
+    float a[4] = {pa::bf16_lo(lo.x), pa::bf16_hi(lo.x), pa::bf16_lo(lo.y), pa::bf16_hi(lo.y)};
+    float b[4] = {pa::bf16_lo(hi.x), pa::bf16_hi(hi.x), pa::bf16_lo(hi.y), pa::bf16_hi(hi.y)};
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+    for (int i = 0; i < 4; ++i) ss = fmaf(b[i], b[i], fmaf(a[i], a[i], ss));
+    // offsets below 16 stay within a half-warp
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-    uint32_t mw[4];  // x as bf16 pairs (exact: x holds bf16 values)
-    if (w != nullptr) {
+    if (wlo != nullptr) {
         const float r = 1.0f / sqrtf(ss * (1.0f / D) + eps);
-        float wv[8];
-        unpack8(*w, wv);
-        // x = bf16(bf16(x * r) * w), two elements per conversion instruction
+        const float wa[4] = {pa::bf16_lo(wlo->x), pa::bf16_hi(wlo->x), pa::bf16_lo(wlo->y), pa::bf16_hi(wlo->y)};
+        const float wb[4] = {pa::bf16_lo(whi->x), pa::bf16_hi(whi->x), pa::bf16_lo(whi->y), pa::bf16_hi(whi->y)};
+        // v = bf16(bf16(v * r) * w), two elements per conversion instruction
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const uint32_t a = pa::pack_bf16x2(x[i] * r, x[i + 1] * r);
-            mw[i / 2] = pa::pack_bf16x2(pa::bf16_lo(a) * wv[i], pa::bf16_hi(a) * wv[i + 1]);
-            x[i] = pa::bf16_lo(mw[i / 2]);
-            x[i + 1] = pa::bf16_hi(mw[i / 2]);
+        for (int i = 0; i < 4; i += 2) {
+            const uint32_t ta = pa::pack_bf16x2(a[i] * r, a[i + 1] * r);
+            const uint32_t ua = pa::pack_bf16x2(pa::bf16_lo(ta) * wa[i], pa::bf16_hi(ta) * wa[i + 1]);
+            a[i] = pa::bf16_lo(ua), a[i + 1] = pa::bf16_hi(ua);
+            const uint32_t tb = pa::pack_bf16x2(b[i] * r, b[i + 1] * r);
+            const uint32_t ub = pa::pack_bf16x2(pa::bf16_lo(tb) * wb[i], pa::bf16_hi(tb) * wb[i + 1]);
+            b[i] = pa::bf16_lo(ub), b[i + 1] = pa::bf16_hi(ub);
         }
-    } else {
-        mw[0] = raw.x, mw[1] = raw.y, mw[2] = raw.z, mw[3] = raw.w;
     }
-    // partner features (i +- 64) live in lane sub ^ 8
-    const uint4 mine = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-    uint4 other;
-    other.x = __shfl_xor_sync(FULL, mine.x, 8);
-    other.y = __shfl_xor_sync(FULL, mine.y, 8);
-    other.z = __shfl_xor_sync(FULL, mine.z, 8);
-    other.w = __shfl_xor_sync(FULL, mine.w, 8);
-    float y[8];
-    unpack8(other, y);
-    float out[8];
-    if (sub < 8) {  // first half: a' = a cos - b sin, with b the partner
+    // a' = a cos - b sin, b' = a sin + b cos (fp32, rounded to bf16)
+    float oa[4], ob[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = fmaf(x[i], c[i], -y[i] * s[i]);
-    } else {        // second half: b' = a sin + b cos, with a the partner
-#pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = fmaf(y[i], s[i], x[i] * c[i]);
+    for (int i = 0; i < 4; ++i) {
+        oa[i] = fmaf(a[i], c[i], -b[i] * s[i]);
+        ob[i] = fmaf(a[i], s[i], b[i] * c[i]);
     }
-    return pack8(out);
+    lo = make_uint2(pa::pack_bf16x2(oa[0], oa[1]), pa::pack_bf16x2(oa[2], oa[3]));
+    hi = make_uint2(pa::pack_bf16x2(ob[0], ob[1]), pa::pack_bf16x2(ob[2], ob[3]));
 }
 
 // Work: one token at a time per CTA (tokens blockIdx.x, + gridDim.x, ...).
@@ -207,9 +183,16 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
         }
     } else {
         // ------------------------------------------------ compute warps
-        uint4 wq = make_uint4(0, 0, 0, 0), wk = wq;
-        if (p.q_weight) wq = *reinterpret_cast<const uint4 *>(p.q_weight + sub * 8);
-        if (p.k_weight) wk = *reinterpret_cast<const uint4 *>(p.k_weight + sub * 8);
+        // this lane's weights: features 4 sub .. +3 and 64 + 4 sub .. +3
+        uint2 wq_lo = make_uint2(0, 0), wq_hi = wq_lo, wk_lo = wq_lo, wk_hi = wq_lo;
+        if (p.q_weight) {
+            wq_lo = *reinterpret_cast<const uint2 *>(p.q_weight + sub * 4);
+            wq_hi = *reinterpret_cast<const uint2 *>(p.q_weight + HALF + sub * 4);
+        }
+        if (p.k_weight) {
+            wk_lo = *reinterpret_cast<const uint2 *>(p.k_weight + sub * 4);
+            wk_hi = *reinterpret_cast<const uint2 *>(p.k_weight + HALF + sub * 4);
+        }
         const int iters = (rows + 2 * COMPUTE_WARPS - 1) / (2 * COMPUTE_WARPS);
         int k = 0;
         for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++k) {
@@ -220,37 +203,44 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
             if (!info.ok) {
                 if (warp == 0 && lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
             } else {
-                const float *cs = reinterpret_cast<const float *>(stage + row_bytes) + (sub & 7) * 8;
-                float c[8], sn[8];
+                const float *cs = reinterpret_cast<const float *>(stage + row_bytes) + sub * 4;
+                float c[4], sn[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) c[i] = cs[i], sn[i] = cs[HALF + i];
+                for (int i = 0; i < 4; ++i) c[i] = cs[i], sn[i] = cs[HALF + i];
                 for (int it = 0; it < iters; ++it) {
                     const int r = (it * COMPUTE_WARPS + warp) * 2 + hw;
                     const bool live = r < rows;
-                    const uint4 raw = live ? *reinterpret_cast<const uint4 *>(stage + r * D * 2 + sub * 16)
-                                           : make_uint4(0, 0, 0, 0);
                     if (r - hw >= p.num_heads + p.kv_heads) {
                         // both rows of the pair are V rows (Hq + Hkv is even, so a pair
                         // never straddles K and V): copied unchanged, no norm or rotation
                         if (live && info.slot != -1) {
                             const int g = r - p.num_heads - p.kv_heads;
                             *reinterpret_cast<uint4 *>(p.v_cache + (int64_t(info.slot) * p.kv_heads + g) * D +
-                                                       sub * 8) = raw;
+                                                       sub * 8) =
+                                *reinterpret_cast<const uint4 *>(stage + r * D * 2 + sub * 16);
                         }
                         continue;
                     }
-                    const bool is_q = r < p.num_heads, is_k = !is_q && r < p.num_heads + p.kv_heads;
-                    const bool has_w = is_q ? p.q_weight != nullptr : (is_k && p.k_weight != nullptr);
-                    const uint4 y = norm_rope8(raw, has_w ? (is_q ? &wq : &wk) : nullptr, p.eps, c, sn, sub);
-                    if (!live) continue;
-                    if (is_q) {
-                        *reinterpret_cast<uint4 *>(p.q_out + t * p.q_out_stride + int64_t(r) * D + sub * 8) = y;
-                    } else if (info.slot != -1) {
-                        const int g = is_k ? r - p.num_heads : r - p.num_heads - p.kv_heads;
-                        uint16_t *dst = (is_k ? p.k_cache : p.v_cache) + (int64_t(info.slot) * p.kv_heads + g) * D +
-                                        sub * 8;
-                        *reinterpret_cast<uint4 *>(dst) = is_k ? y : raw;
+                    uint2 lo = make_uint2(0, 0), hi = lo;
+                    if (live) {
+                        lo = *reinterpret_cast<const uint2 *>(stage + r * D * 2 + sub * 8);
+                        hi = *reinterpret_cast<const uint2 *>(stage + r * D * 2 + HALF * 2 + sub * 8);
                     }
+                    const bool is_q = r < p.num_heads;
+                    const bool has_w = is_q ? p.q_weight != nullptr : p.k_weight != nullptr;
+                    norm_rope_pairs(lo, hi, has_w ? (is_q ? &wq_lo : &wk_lo) : nullptr, is_q ? &wq_hi : &wk_hi, p.eps,
+                                    c, sn);
+                    if (!live) continue;
+                    uint16_t *dst;
+                    if (is_q) {
+                        dst = p.q_out + t * p.q_out_stride + int64_t(r) * D;
+                    } else if (info.slot != -1) {
+                        dst = p.k_cache + (int64_t(info.slot) * p.kv_heads + (r - p.num_heads)) * D;
+                    } else {
+                        continue;
+                    }
+                    *reinterpret_cast<uint2 *>(dst + sub * 4) = lo;
+                    *reinterpret_cast<uint2 *>(dst + HALF + sub * 4) = hi;
                 }
             }
             __syncwarp();
