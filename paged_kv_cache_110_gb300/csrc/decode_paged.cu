@@ -288,10 +288,20 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
             unpack8(kr[i], kf);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float acc = 0.f;
+                if constexpr (FP8) {
+                    // fp8 pools are bound by instruction issue (each element also needs a
+                    // conversion): paired fp32 FMAs, two partial sums, half the FMAs
+                    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-                x[i * G + h] = acc;
+                    for (int e = 0; e < 8; e += 2)
+                        pa::sm100::ffma2(a0, a1, qf[h][e], qf[h][e + 1], kf[e], kf[e + 1], a0, a1);
+                    x[i * G + h] = a0 + a1;
+                } else {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+                    x[i * G + h] = acc;
+                }
             }
         }
         xpose_step<V, 8>(x, c);
@@ -338,8 +348,14 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
                 const int idx = i * G + h;
                 const int src_c = (G == 1) ? 2 * i : idx / R;
                 const float pv = __shfl_sync(FULL, pr[(G == 1) ? 0 : idx % R], src_c, 16);
+                if constexpr (FP8) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pv, vf[e], o[h][e]);
+                    for (int e = 0; e < 8; e += 2)
+                        pa::sm100::ffma2(o[h][e], o[h][e + 1], pv, pv, vf[e], vf[e + 1], o[h][e], o[h][e + 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pv, vf[e], o[h][e]);
+                }
             }
         }
     }
