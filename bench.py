@@ -52,8 +52,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 # DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
 # valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha256": "1be3db8234954f1e66cec316300674351ccd157d335a9cdcb1337524af9faf0b",
-               "bytes_per_call": 587_065_088 + 6_971_136, "kernel": "decode_split_kernel<2, 0>"}
+NCU_TRAFFIC = {"source_sha256": "de5643ab3809b566bd2d818eff1c6470ba994e5120f1bbb3acd9089501d2fde5",
+               "bytes_per_call": 587_109_888 + 6_950_912, "kernel": "decode_split_kernel<2, 0>"}
 
 
 def _file_sha(path):

@@ -95,6 +95,28 @@ def test_prefill_varlen_16k():
     _prefill_case(wl.varlen_prefill(device=dev()))
 
 
+def test_prefill_out_aligned_to_16_bytes_only():
+    """An output buffer that starts 16 bytes past a 32-byte boundary (allowed:
+    the entry point asks for 16) takes the 16-byte-store epilogue instead of
+    the 32-byte one; both must give the same bits."""
+    batch = wl.varlen_prefill(device=dev())
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    st = Status(kc.device)
+    gpu_store(batch, kc, vc, st)
+    ref = gpu_prefill(batch, kc, vc, paged=True, status=st)
+    n = ref.numel()
+    buf = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device=kc.device)
+    out = buf[8:8 + n].view(ref.shape)  # 8 bf16 = 16 bytes in
+    assert out.data_ptr() % 32 == 16
+    d = kc.device
+    pa().pa_prefill_paged(batch.tokens.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d),
+                          int(batch.query_lens.max()), int(batch.context_lens.max()), batch.scale, out,
+                          dev_status=st.t, k_cache=kc, v_cache=vc, block_table=i32(batch.block_tables, d))
+    assert st.value() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all()
+
+
 @pytest.mark.parametrize("growth", [0.02, 0.002], ids=["jump_every_tile", "slow_growth"])
 @pytest.mark.parametrize("lens", [[700, 1024, 129, 300], [1600]], ids=["batch", "one_long_split"])
 def test_prefill_growing_scores_rescale(growth, lens):
