@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 mbar_arrive(bar(B_IRF + slot));
             }
             if (w < 0) break;
-            // the item's Q tiles into Q buffers 2n and 2n+1 of the ring of three
+            // the item's Q tiles into Q buffers 2n and 2n+1 (mod 2)
             // (rows past the sequence are other sequences' rows or TMA zero fill:
             // their results are not stored)
             bool ok = true;
