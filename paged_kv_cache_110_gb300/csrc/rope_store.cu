@@ -211,8 +211,9 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
                     const int r = (it * COMPUTE_WARPS + warp) * 2 + hw;
                     const bool live = r < rows;
                     if (r - hw >= p.num_heads + p.kv_heads) {
-                        // both rows of the pair are V rows (Hq + Hkv is even, so a pair
-                        // never straddles K and V): copied unchanged, no norm or rotation
+                        // both rows of the pair are V rows: copied unchanged, no norm or
+                        // rotation (a pair that holds a K and a V row, possible when
+                        // Hq + Hkv is odd, goes through the path below)
                         if (live && info.slot != -1) {
                             const int g = r - p.num_heads - p.kv_heads;
                             *reinterpret_cast<uint4 *>(p.v_cache + (int64_t(info.slot) * p.kv_heads + g) * D +
@@ -226,6 +227,21 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
                         lo = *reinterpret_cast<const uint2 *>(stage + r * D * 2 + sub * 8);
                         hi = *reinterpret_cast<const uint2 *>(stage + r * D * 2 + HALF * 2 + sub * 8);
                     }
+                    if (r - hw + 1 == p.num_heads + p.kv_heads) {
+                        // the pair of the last K row and the first V row (Hq + Hkv odd):
+                        // both half-warps take part in the norm's shuffles, the V half
+                        // stores its row unchanged
+                        const uint2 raw_lo = lo, raw_hi = hi;
+                        norm_rope_pairs(lo, hi, p.k_weight ? &wk_lo : nullptr, &wk_hi, p.eps, c, sn);
+                        if (live && info.slot != -1) {
+                            const int g = hw == 0 ? r - p.num_heads : r - p.num_heads - p.kv_heads;
+                            uint16_t *dst = (hw == 0 ? p.k_cache : p.v_cache) + (int64_t(info.slot) * p.kv_heads + g) * D;
+                            *reinterpret_cast<uint2 *>(dst + sub * 4) = hw == 0 ? lo : raw_lo;
+                            *reinterpret_cast<uint2 *>(dst + HALF + sub * 4) = hw == 0 ? hi : raw_hi;
+                        }
+                        continue;
+                    }
+                    // Q or K rows only
                     const bool is_q = r < p.num_heads;
                     const bool has_w = is_q ? p.q_weight != nullptr : p.k_weight != nullptr;
                     norm_rope_pairs(lo, hi, has_w ? (is_q ? &wq_lo : &wk_lo) : nullptr, is_q ? &wq_hi : &wk_hi, p.eps,

@@ -34,8 +34,6 @@ def _built():
     __graft_entry__.build()
 
 
-
-
 def _values(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -118,6 +116,16 @@ def test_decode_sized_call_at_late_positions():
     batch = wl.paged_batch(wl.SEED_BASE + 62, ctx, np.ones(256, int), 256, device=dev())
     slots, pos = batch.slot_mapping, batch.positions
     _compare(_run(batch, slots, pos), slots, "decode-sized")
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (2, 1), (4, 1), (8, 1), (16, 4), (32, 8), (64, 8)])
+def test_head_configurations(hq, hkv):
+    """Every supported head count, including the odd row totals of one KV head
+    (Hq + 1 rows of Q and K, then one V row), where a K row and a V row are
+    processed together."""
+    batch = wl.paged_batch(wl.SEED_BASE + 66, [33, 70], [33, 70], 16, num_heads=hq, num_kv_heads=hkv, device=dev())
+    slots, pos = batch.slot_mapping, batch.positions
+    _compare(_run(batch, slots, pos), slots, f"hq={hq} hkv={hkv}")
 
 
 def test_rope_only_without_norm_weights():
