@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) prefill_scan_kernel(const int32_
                                                                     int32_t *cu_q, int32_t *cu_k, int32_t *max_seqlens,
                                                                     int32_t *status)
 {
+    pa::grid_dependency_wait();  // launched programmatically: the counts may come from the kernel before
+    pa::grid_dependents_launch();
     __shared__ int64_t sums[32];
     __shared__ int maxes[32];
     __shared__ int64_t last[2];
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(256) prefill_expand_kernel(const int32_t *seq_
                                                              int32_t *positions, int32_t *slot_mapping,
                                                              int64_t max_tokens, int32_t *status)
 {
+    pa::grid_dependency_wait();  // cu_seqlens_q from the scan
     for (int b = blockIdx.x; b < num_seqs; b += gridDim.x) {
         const SeqCounts c = counts(seq_lens, num_cached, num_scheduled, b);
         const int64_t offset = cu_q[b];
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(256) decode_meta_kernel(const int32_t *seq_len
                                                           int64_t num_blocks, int32_t *positions, int32_t *context_lens,
                                                           int32_t *slot_mapping, int32_t *status)
 {
+    pa::grid_dependency_wait();  // launched programmatically
     for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < num_seqs; b += gridDim.x * blockDim.x) {
         const int len = seq_lens[b];
         if (len <= 0) {  // padding row
@@ -191,13 +195,13 @@ extern "C" pa_status pa_prepare_prefill(const int32_t *seq_lens, const int32_t *
         return PA_ERR_INVALID_ARG;
     if (!metadata_shape_ok(max_blocks, block_size, num_blocks)) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    prefill_scan_kernel<<<1, SCAN_THREADS, 0, s>>>(seq_lens, num_cached, num_scheduled, num_seqs, cu_seqlens_q,
-                                                   cu_seqlens_k, max_seqlens, dev_status);
+    pa::launch_pdl(prefill_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, s, seq_lens, num_cached, num_scheduled,
+                   num_seqs, cu_seqlens_q, cu_seqlens_k, max_seqlens, dev_status);
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
     const int grid = num_seqs < sms * 8 ? num_seqs : sms * 8;
-    prefill_expand_kernel<<<grid, 256, 0, s>>>(seq_lens, num_cached, num_scheduled, num_seqs, block_table, max_blocks,
-                                               block_size, num_blocks, cu_seqlens_q, positions, slot_mapping,
-                                               max_tokens, dev_status);
+    pa::launch_pdl(prefill_expand_kernel, dim3(grid), dim3(256), 0, s, seq_lens, num_cached, num_scheduled, num_seqs,
+                   block_table, max_blocks, block_size, num_blocks, static_cast<const int32_t *>(cu_seqlens_q),
+                   positions, slot_mapping, max_tokens, dev_status);
     return pa::launch_status();
 }
 
@@ -211,8 +215,8 @@ extern "C" pa_status pa_prepare_decode(const int32_t *seq_lens, int num_seqs, co
     if (!seq_lens || !block_table || !positions || !context_lens || !slot_mapping) return PA_ERR_INVALID_ARG;
     if (!metadata_shape_ok(max_blocks, block_size, num_blocks)) return PA_ERR_INVALID_ARG;
     const int grid = (num_seqs + 255) / 256;
-    decode_meta_kernel<<<grid < 1024 ? grid : 1024, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        seq_lens, num_seqs, block_table, max_blocks, block_size, num_blocks, positions, context_lens, slot_mapping,
-        dev_status);
+    pa::launch_pdl(decode_meta_kernel, dim3(grid < 1024 ? grid : 1024), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                   seq_lens, num_seqs, block_table, max_blocks, block_size, num_blocks, positions, context_lens,
+                   slot_mapping, dev_status);
     return pa::launch_status();
 }

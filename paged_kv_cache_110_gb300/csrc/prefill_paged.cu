@@ -300,6 +300,8 @@ __device__ __forceinline__ void mask_tail(uint32_t (&s)[N], int base, int limit)
 template <bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
+    // launched programmatically: the KV write before it must be complete
+    pa::grid_dependency_wait();
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
@@ -809,6 +811,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 constexpr int MERGE_ROWS = 16;
 __global__ void __launch_bounds__(MERGE_ROWS * 16) prefill_merge_kernel(const __grid_constant__ TcParams p)
 {
+    pa::grid_dependency_wait();  // the shares of the split kernel
     const int a = blockIdx.y;
     const int r = blockIdx.z * MERGE_ROWS + int(threadIdx.x >> 4);
     const int c8 = int(threadIdx.x & 15) * 8;  // this thread's first column
@@ -1019,11 +1022,12 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
     const dim3 grid(unsigned(units < sms ? units : sms));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.kv_splits > 1)
-        prefill_tc_kernel<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+        pa::launch_pdl(prefill_tc_kernel<true>, grid, dim3(NTHREADS), SMEM_BYTES, s, p);
     else
-        prefill_tc_kernel<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+        pa::launch_pdl(prefill_tc_kernel<false>, grid, dim3(NTHREADS), SMEM_BYTES, s, p);
     if (pl.kv_splits > 1)
-        prefill_merge_kernel<<<dim3(unsigned(pl.items), QT, BM / MERGE_ROWS), MERGE_ROWS * 16, 0, s>>>(p);
+        pa::launch_pdl(prefill_merge_kernel, dim3(unsigned(pl.items), QT, BM / MERGE_ROWS), dim3(MERGE_ROWS * 16), 0,
+                       s, p);
     return pa::launch_status();
 }
 
