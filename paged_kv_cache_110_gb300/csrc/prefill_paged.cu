@@ -731,55 +731,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             ++no;
             if (!ok) break;
             tc_fence_after();
+            // the whole O row in one TMEM load (one wait, not one per half)
+            uint32_t o[128];
+            tmem_ld128_sync(ocol, o);
             if (SPLIT && it.split) {
                 // a share of a split item: unnormalised O and (max, sum) for the merge
-                const int64_t row = (int64_t(w) * QT + a) * BM + r;
+                if (r < it.rows[a]) {
+                    const int64_t row = (int64_t(w) * QT + a) * BM + r;
+                    float *dst = p.ws_o + row * D;  // 256-byte aligned rows
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t o[64];
-                    tmem_ld64_sync(ocol + hf * 64, o);
-                    if (r < it.rows[a]) {
-                        float *dst = p.ws_o + row * D + hf * 64;  // 256-byte aligned rows
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            uint32_t w8[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) w8[e] = o[8 * v + e];
-                            st_global_v8(dst + 8 * v, w8);
-                        }
-                    }
-                }
-                if (r < it.rows[a]) p.ws_ml[row] = make_float2(m_used, l);
-                continue;
-            }
-            const float inv = 1.f / l;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t o[64];
-                tmem_ld64_sync(ocol + hf * 64, o);
-                if (r < it.rows[a] && p.out_v8) {
-                    uint16_t *dst = p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D + hf * 64;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 16; ++v) {
                         uint32_t w8[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            w8[e] = pa::pack_bf16x2(__uint_as_float(o[16 * v + 2 * e]) * inv,
-                                                    __uint_as_float(o[16 * v + 2 * e + 1]) * inv);
-                        st_global_v8(dst + 16 * v, w8);
+                        for (int e = 0; e < 8; ++e) w8[e] = o[8 * v + e];
+                        st_global_v8(dst + 8 * v, w8);
                     }
-                } else if (r < it.rows[a]) {
-                    uint4 *d4 =
-                        reinterpret_cast<uint4 *>(p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D);
+                    p.ws_ml[row] = make_float2(m_used, l);
+                }
+                continue;
+            }
+            if (r >= it.rows[a]) continue;
+            const float inv = 1.f / l;
+            uint16_t *dst = p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D;
+            if (p.out_v8) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        uint4 u;
-                        u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        d4[hf * 8 + v] = u;
-                    }
+                for (int v = 0; v < 8; ++v) {
+                    uint32_t w8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w8[e] = pa::pack_bf16x2(__uint_as_float(o[16 * v + 2 * e]) * inv,
+                                                __uint_as_float(o[16 * v + 2 * e + 1]) * inv);
+                    st_global_v8(dst + 16 * v, w8);
+                }
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    uint4 u;
+                    u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    d4[v] = u;
                 }
             }
         }
