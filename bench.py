@@ -205,9 +205,12 @@ class ClockSampler:
 
 class DecodeStep:
     """28 layers of (KV write of the new tokens, paged decode) over distinct
-    per-layer pools that share one set of block tables."""
+    per-layer pools that share one set of block tables.  With `fused` (the
+    default) each layer is one pa_store_decode_paged call; otherwise
+    pa_store_kvcache then pa_decode_paged."""
 
-    def __init__(self, device, seed=wl.SEED_BASE + 2, layers=LAYERS, keep_host_layer0=False):
+    def __init__(self, device, seed=wl.SEED_BASE + 2, layers=LAYERS, keep_host_layer0=False, fused=True):
+        self.fused = fused
         from paged_kv_cache_110_gb300 import binding as pa
         self.pa = pa
         self.dev = device
@@ -237,21 +240,34 @@ class DecodeStep:
         self.store_bytes = store_bytes(self.B)
         self.step_bytes = layers * (self.decode_bytes + self.store_bytes)
 
+    @property
+    def call_bytes(self):
+        """Algorithmic bytes of the call the events time: the fused KV write +
+        decode, or the decode alone."""
+        return self.decode_bytes + (self.store_bytes if self.fused else 0)
+
     def run(self, events=None):
         pa = self.pa
         for l in range(self.layers):
             t = self.tokens[l]
-            pa.pa_store_kvcache(t.k, t.v, self.k_cache[l], self.v_cache[l], self.slots)
+            if not self.fused:
+                pa.pa_store_kvcache(t.k, t.v, self.k_cache[l], self.v_cache[l], self.slots)
             if events is not None:
                 events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                 events[-1][0].record()
-            pa.pa_decode_paged(t.q, self.k_cache[l], self.v_cache[l], self.tables, self.ctx_t, self.max_ctx,
-                               wl.SCALE, self.out[l], self.ws)
+            if self.fused:
+                pa.pa_store_decode_paged(t.q, t.k, t.v, self.k_cache[l], self.v_cache[l], self.tables, self.ctx_t,
+                                         self.max_ctx, wl.SCALE, self.out[l], self.ws)
+            else:
+                pa.pa_decode_paged(t.q, self.k_cache[l], self.v_cache[l], self.tables, self.ctx_t, self.max_ctx,
+                                   wl.SCALE, self.out[l], self.ws)
             if events is not None:
                 events[-1][1].record()
 
     def launches_per_step(self):
-        return self.layers * (1 + (2 if self._multi_split() else 1))
+        # per layer: the decode kernel, its merge when the keys are split, and the
+        # KV-write kernel unless it is fused into the decode
+        return self.layers * ((0 if self.fused else 1) + (2 if self._multi_split() else 1))
 
     def _multi_split(self):
         # the library uses a merge kernel whenever a workspace is needed
@@ -274,20 +290,32 @@ class E2EStep:
         a, b = HQ * D, (HQ + HKV) * D
         self.views = [(q[:, :a].view(-1, HQ, D), q[:, a:b].view(-1, HKV, D), q[:, b:].view(-1, HKV, D))
                       for q in self.d_qkv]
+        meta = (self.h_tables, self.h_ctx) if step.fused else (self.h_slots, self.h_tables, self.h_ctx)
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_qkv) + \
-            sum(t.numel() * t.element_size() for t in (self.h_slots, self.h_tables, self.h_ctx))
+            sum(t.numel() * t.element_size() for t in meta)
         self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
 
-    def run(self):
+    def layer(self, l):
+        """Layer l's C-ABI call(s) on the current stream."""
         s, pa = self.s, self.s.pa
-        s.slots.copy_(self.h_slots, non_blocking=True)
+        q, k, v = self.views[l]
+        if s.fused:
+            pa.pa_store_decode_paged(q, k, v, s.k_cache[l], s.v_cache[l], s.tables, s.ctx_t, s.max_ctx, wl.SCALE,
+                                     s.out[l], s.ws)
+        else:
+            pa.pa_store_kvcache(k, v, s.k_cache[l], s.v_cache[l], s.slots)
+            pa.pa_decode_paged(q, s.k_cache[l], s.v_cache[l], s.tables, s.ctx_t, s.max_ctx, wl.SCALE, s.out[l],
+                               s.ws)
+
+    def run(self):
+        s = self.s
+        if not s.fused:
+            s.slots.copy_(self.h_slots, non_blocking=True)
         s.tables.copy_(self.h_tables, non_blocking=True)
         s.ctx_t.copy_(self.h_ctx, non_blocking=True)
         for l in range(s.layers):
             self.d_qkv[l].copy_(self.h_qkv[l], non_blocking=True)
-            q, k, v = self.views[l]
-            pa.pa_store_kvcache(k, v, s.k_cache[l], s.v_cache[l], s.slots)
-            pa.pa_decode_paged(q, s.k_cache[l], s.v_cache[l], s.tables, s.ctx_t, s.max_ctx, wl.SCALE, s.out[l], s.ws)
+            self.layer(l)
             self.h_out[l].copy_(s.out[l], non_blocking=True)
 
 
@@ -316,7 +344,8 @@ class E2EGraphStep:
                 ev_in = [torch.cuda.Event() for _ in range(s.layers)]
                 ev_out = [torch.cuda.Event() for _ in range(s.layers)]
                 with torch.cuda.stream(h2d):
-                    s.slots.copy_(e.h_slots, non_blocking=True)
+                    if not s.fused:
+                        s.slots.copy_(e.h_slots, non_blocking=True)
                     s.tables.copy_(e.h_tables, non_blocking=True)
                     s.ctx_t.copy_(e.h_ctx, non_blocking=True)
                     for l in range(s.layers):
@@ -324,10 +353,7 @@ class E2EGraphStep:
                         ev_in[l].record(h2d)
                 for l in range(s.layers):
                     cap.wait_event(ev_in[l])
-                    q, k, v = e.views[l]
-                    s.pa.pa_store_kvcache(k, v, s.k_cache[l], s.v_cache[l], s.slots)
-                    s.pa.pa_decode_paged(q, s.k_cache[l], s.v_cache[l], s.tables, s.ctx_t, s.max_ctx, wl.SCALE,
-                                         s.out[l], s.ws)
+                    e.layer(l)
                     ev_out[l].record(cap)
                 with torch.cuda.stream(d2h):
                     for l in range(s.layers):
@@ -854,6 +880,20 @@ def main():
         graph.replay()
     torch.cuda.synchronize()
 
+    # for comparison: the same step with the KV write as its own launch before
+    # each decode (pa_store_kvcache + pa_decode_paged), also graph-captured
+    step.fused = False
+    graph_unfused = torch.cuda.CUDAGraph()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph_unfused):
+            step.run()
+    torch.cuda.current_stream().wait_stream(side)
+    step.fused = True
+    for _ in range(args.warmup):
+        graph_unfused.replay()
+    torch.cuda.synchronize()
+
     events = []
     with ClockSampler(gpu_index) as clocks:
         clocks.wait_first()
@@ -863,15 +903,17 @@ def main():
         # beside it: the same kernels launched one by one, with CUDA events
         # around every decode call for the roofline
         elapsed = time_region(lambda: step.run(events), args.steps, world)
+        unfused_el = time_region(graph_unfused.replay, args.steps, world)
         h1 = time.time()
         time.sleep(0.3)
-    del graph
+    del graph, graph_unfused
     t_max, bytes_all = reduce_max_sum(world, g_el, float(step.step_bytes * args.steps))
     value = bytes_all / t_max / 1e9
     eager_t, eager_bytes = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
     eager_value = eager_bytes / eager_t / 1e9
+    unfused_t, unfused_bytes = reduce_max_sum(world, unfused_el, float(step.step_bytes * args.steps))
     decode_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
-    achieved = step.decode_bytes / decode_s / 1e9
+    achieved = step.call_bytes / decode_s / 1e9
 
     e2e = E2EStep(step)
     for _ in range(2):
@@ -892,7 +934,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "decode batch x 28 layers: 256 seqs, context_lens U[100,1024], block_size 256, "
-                               "16q/8kv x 128 bf16; per layer KV write of 256 tokens + paged decode",
+                               "16q/8kv x 128 bf16; per layer KV write of 256 tokens + paged decode "
+                               "(one pa_store_decode_paged call)",
                    "layers": step.layers, "seqs": step.B, "sum_context": int(step.ctx.sum()),
                    "l2": "inputs larger than L2: 28 distinct layer pools (%.1f GB)" %
                          (step.layers * 2 * step.layout.num_blocks * 256 * ROW_BYTES / 1e9),
@@ -903,16 +946,19 @@ def main():
         "timing": "the 28-layer step captured once in a CUDA graph and replayed K times (how a serving engine "
                   "runs decode); the same kernels launched one by one from Python are reported under 'eager'",
         "eager": {"value": eager_value, "unit": "GB/s", "ms_per_step": eager_t / args.steps * 1e3},
+        "unfused": {"value": unfused_bytes / unfused_t / 1e9, "unit": "GB/s",
+                    "ms_per_step": unfused_t / args.steps * 1e3,
+                    "how": "the same step, graph-captured, with pa_store_kvcache and pa_decode_paged per layer"},
         "e2e": {"value": e2e_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": e2e.h2d,
                 "d2h_bytes_per_step": e2e.d2h, "ms_per_step": e2e_t / args.steps * 1e3,
                 "how": "C-ABI calls of the step with pinned-host copies in and out, captured in a CUDA graph with "
                        "the copies on their own streams; every copy is inside each replay",
                 "eager_ms_per_step": e2e_eager_t / args.steps * 1e3},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode_paged (split + merge kernels)",
+        "roofline": {"bound": "hbm", "kernel": "pa_store_decode_paged (split-KV kernel with the KV write, merge)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
                      "traffic": traffic, "traffic_kernel": NCU_TRAFFIC["kernel"],
-                     "algorithmic_bytes_per_call": step.decode_bytes,
+                     "algorithmic_bytes_per_call": step.call_bytes,
                      "us_per_call": decode_s * 1e6},
         "clocks": clocks.summary(h0, h1 + 0.25),
     }

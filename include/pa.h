@@ -279,6 +279,32 @@ pa_status pa_decode_paged(const void *q, int64_t q_stride_seq,
                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * The decode step's KV write and paged decode in one launch ("大模型推理入门与
+ * nano-vLLM 源码详解" §13.1 and §13.5: store_kvcache then attention over the
+ * cache).  For every sequence b with context_lens[b] > 0, k_new[b] and
+ * v_new[b] (the token at position p = context_lens[b] - 1) are written to pool
+ * row block_table[b][p / block_size] * block_size + p % block_size, and q[b]
+ * attends to keys 0 .. p as in pa_decode_paged.  The result (out and the pool)
+ * is the same as pa_store_kvcache with that row as slot_mapping[b], followed
+ * by pa_decode_paged with the same arguments.
+ *
+ *   k_new, v_new  [num_seqs, num_kv_heads, head_dim] bf16, sequence stride
+ *                 kv_new_stride_seq elements (a multiple of 8, at least
+ *                 num_kv_heads * head_dim); 16-byte aligned.
+ *   k_cache, v_cache  bf16 pools, written.
+ *   Every other argument, the workspace and the errors as pa_decode_paged;
+ *   an invalid block id of the new token's row sets PA_ERR_BOUNDS and that
+ *   row is neither written nor read.  Rows of padded sequences (context 0)
+ *   are not written.
+ */
+pa_status pa_store_decode_paged(const void *q, int64_t q_stride_seq, const void *k_new, const void *v_new,
+                                int64_t kv_new_stride_seq, void *k_cache, void *v_cache, int64_t num_blocks,
+                                int block_size, const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *context_lens, int num_seqs, int max_context_len, int num_heads,
+                                int num_kv_heads, int head_dim, float scale, void *out, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * fp8 KV cache ("大模型推理入门与 nano-vLLM 源码详解" §17.3 names the KV
  * precision as the lever for longer contexts; "VLLM on Fain的Blog" counts FP8
  * at one byte per element.  The pages fix no format; this library's is the

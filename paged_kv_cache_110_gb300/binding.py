@@ -19,7 +19,8 @@ __all__ = [
     "PaError", "lib", "pa_status_string", "pa_abi_version", "pa_kv_bytes_per_token",
     "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_norm_rope_store_kvcache", "pa_rope_cos_sin_table",
     "pa_prepare_prefill", "pa_prepare_decode", "pa_prefill_workspace_bytes", "pa_prefill_paged",
-    "pa_decode_workspace_bytes", "pa_decode_paged", "pa_decode_paged_fp8", "pa_decode_paged_noalloc",
+    "pa_decode_workspace_bytes", "pa_decode_paged", "pa_store_decode_paged", "pa_decode_paged_fp8",
+    "pa_decode_paged_noalloc",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
@@ -69,6 +70,9 @@ def _load() -> ctypes.CDLL:
     L.pa_decode_paged.restype = i32
     L.pa_decode_paged.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp,
                                   vp, sz, vp, vp]
+    L.pa_store_decode_paged.restype = i32
+    L.pa_store_decode_paged.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                                        f32, vp, vp, sz, vp, vp]
     L.pa_decode_paged_noalloc.restype = i32
     L.pa_decode_paged_noalloc.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32,
                                           vp, vp, vp]
@@ -333,6 +337,33 @@ def pa_decode_paged(q, k_cache, v_cache, block_table, context_lens, max_context_
                                float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                _stream(stream)),
            "pa_decode_paged")
+
+
+def pa_store_decode_paged(q, k_new, v_new, k_cache, v_cache, block_table, context_lens, max_context_len, scale, out,
+                          workspace, dev_status=None, stream=None):
+    """The decode step's KV write and decode in one launch: k_new / v_new
+    [B, Hkv, 128] (the token at position context_lens[b] - 1, same sequence
+    stride) go to that position's pool row, then decode as pa_decode_paged."""
+    hq, qs = _bf16_rows(q, "q")
+    hk, ks = _bf16_rows(k_new, "k_new")
+    hv, vs = _bf16_rows(v_new, "v_new")
+    nb, bs, hkv, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    _i32(block_table, "block_table")
+    _i32(context_lens, "context_lens")
+    b = q.shape[0]
+    if hk != hkv or hv != hkv or ks != vs or k_new.shape[0] != b or v_new.shape[0] != b:
+        raise ValueError("k_new / v_new must be [B, Hkv, D] bf16 with one sequence stride")
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (b, hq, d):
+        raise ValueError("out must be a contiguous bf16 [B, Hq, D] tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != b or context_lens.numel() != b:
+        raise ValueError("block_table / context_lens do not match q")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_store_decode_paged(_ptr(q), qs, _ptr(k_new), _ptr(v_new), ks, _ptr(k_cache), _ptr(v_cache), nb,
+                                     bs, _ptr(block_table), block_table.shape[1], _ptr(context_lens), b,
+                                     int(max_context_len), hq, hkv, d, float(scale), _ptr(out), _ptr(workspace),
+                                     ws_bytes, _ptr(dev_status), _stream(stream)),
+           "pa_store_decode_paged")
 
 
 def pa_decode_paged_noalloc(q, k_cache, v_cache, block_table, context_lens, max_context_len, scale, out,

@@ -62,6 +62,9 @@ struct DecodeParams {
     float scale_log2;   // scale * log2(e) (times the K scale for fp8 pools)
     float out_scale;    // 1, or the V scale for fp8 pools
     uint16_t *out;
+    const uint16_t *k_new;  // fused KV write: the step's new K / V rows [num_seqs][kv_heads][D], or null
+    const uint16_t *v_new;
+    int64_t kv_new_stride;  // elements between sequences' rows of k_new / v_new
     float *ws_o;      // [num_seqs][max_splits][num_heads][D]
     float2 *ws_ml;    // [num_seqs][max_splits][num_heads] (max, sum), base-2
     int split_len;
@@ -143,6 +146,7 @@ struct KvRow {
     using Raw = uint4;
     using Elem = uint16_t;
     static __device__ __forceinline__ Raw load(const Elem *p) { return pa::ld_stream16(p); }
+    static __device__ __forceinline__ Raw load_l2(const Elem *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
     static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
 };
 template <>
@@ -150,6 +154,7 @@ struct KvRow<true> {
     using Raw = uint2;
     using Elem = uint8_t;
     static __device__ __forceinline__ Raw load(const Elem *p) { return ld_stream8(p); }
+    static __device__ __forceinline__ Raw load_l2(const Elem *p) { return __ldcg(reinterpret_cast<const uint2 *>(p)); }
     static __device__ __forceinline__ Raw zero() { return make_uint2(0, 0); }
 };
 
@@ -221,6 +226,31 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     const int t0 = s * p.split_len;
     const int t1 = min(ctx, t0 + p.split_len);
     const int64_t row_elems = int64_t(p.kv_heads) * D;
+    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+
+    // Fused KV write (bf16 pools): the sequence's last split stores the step's new
+    // token, position ctx - 1, at its pool row (warp g: head g, lanes 0-15 K,
+    // 16-31 V) before any of its warps reads.  Only this CTA reads that row in
+    // this launch, after the barrier below, and the chunk that holds it is read
+    // through L2 (ld.global.cg), not the read-only path the other chunks use.
+    int new_tok = -1;  // position written by this launch, or -1
+    if constexpr (!FP8) {
+        if (p.k_new != nullptr && s == nsplit - 1) {  // the same for the whole CTA
+            new_tok = ctx - 1;
+            if (sub == 0) {
+                const int32_t phys = table[new_tok / p.block_size];
+                if (phys >= 0 && int64_t(phys) < p.num_blocks) {
+                    const int64_t row = int64_t(phys) * p.block_size + new_tok % p.block_size;
+                    const uint16_t *src = (half ? p.v_new : p.k_new) + int64_t(b) * p.kv_new_stride + g * D + 8 * c;
+                    uint16_t *dst = static_cast<uint16_t *>(const_cast<void *>(half ? p.v_cache : p.k_cache)) +
+                                    row * row_elems + g * D + 8 * c;
+                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                }
+                // an invalid block id is reported by the loop below, which skips that chunk
+            }
+            __syncthreads();
+        }
+    }
 
     float qf[G][8];
 #pragma unroll
@@ -240,7 +270,6 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
     }
 
-    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
     for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
         const int32_t phys = table[cb / p.block_size];
         if (phys < 0 || int64_t(phys) >= p.num_blocks) {
@@ -269,14 +298,28 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
 
         typename KV::Raw kr[8], vr[8];
+        if (!FP8 && unsigned(new_tok - cb) < unsigned(CHUNK)) {
+            // the chunk holding the row this launch wrote: coherent loads through L2
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < nvalid) {
-                kr[i] = KV::load(kp + i * row_elems);
-                vr[i] = KV::load(vp + i * row_elems);
-            } else {
-                kr[i] = KV::zero();
-                vr[i] = KV::zero();
+            for (int i = 0; i < 8; ++i) {
+                if (i < nvalid) {
+                    kr[i] = KV::load_l2(kp + i * row_elems);
+                    vr[i] = KV::load_l2(vp + i * row_elems);
+                } else {
+                    kr[i] = KV::zero();
+                    vr[i] = KV::zero();
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < nvalid) {
+                    kr[i] = KV::load(kp + i * row_elems);
+                    vr[i] = KV::load(vp + i * row_elems);
+                } else {
+                    kr[i] = KV::zero();
+                    vr[i] = KV::zero();
+                }
             }
         }
 
@@ -536,7 +579,8 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
                       float k_scale, float v_scale, int64_t num_blocks, int block_size, const int32_t *block_table,
                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int max_context_len,
                       int num_heads, int num_kv_heads, int head_dim, float scale, void *out, void *workspace,
-                      size_t workspace_bytes_given, int32_t *dev_status, void *stream)
+                      size_t workspace_bytes_given, int32_t *dev_status, void *stream, const void *k_new = nullptr,
+                      const void *v_new = nullptr, int64_t kv_new_stride = 0)
 {
     pa_status st = check_args(q, q_stride_seq, k_cache, v_cache, num_blocks, block_size, block_table,
                               max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
@@ -565,6 +609,9 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
     p.scale_log2 = scale * LOG2E * k_scale;
     p.out_scale = v_scale;
     p.out = static_cast<uint16_t *>(out);
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.kv_new_stride = kv_new_stride;
     const size_t n = size_t(num_seqs) * (plan.max_splits > 0 ? plan.max_splits : 1) * num_heads;
     p.ws_o = static_cast<float *>(workspace);
     p.ws_ml = need > 0 ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
@@ -607,6 +654,28 @@ extern "C" pa_status pa_decode_paged(const void *q, int64_t q_stride_seq, const 
     return decode_impl(q, q_stride_seq, k_cache, v_cache, false, 1.f, 1.f, num_blocks, block_size, block_table,
                        max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
                        head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream);
+}
+
+// The decode step's KV write and decode in one launch: the sequence's last
+// split stores k_new[b] / v_new[b] at the pool row of position
+// context_lens[b] - 1 (found through the block table, as the decode step's
+// slot is) and decodes with it.
+extern "C" pa_status pa_store_decode_paged(const void *q, int64_t q_stride_seq, const void *k_new, const void *v_new,
+                                           int64_t kv_new_stride_seq, void *k_cache, void *v_cache,
+                                           int64_t num_blocks, int block_size, const int32_t *block_table,
+                                           int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                           int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                                           float scale, void *out, void *workspace, size_t workspace_bytes_given,
+                                           int32_t *dev_status, void *stream)
+{
+    if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr || !pa::aligned(k_new, 16) ||
+                         !pa::aligned(v_new, 16) || kv_new_stride_seq < int64_t(num_kv_heads) * head_dim ||
+                         kv_new_stride_seq % 8 != 0))
+        return PA_ERR_INVALID_ARG;
+    return decode_impl(q, q_stride_seq, k_cache, v_cache, false, 1.f, 1.f, num_blocks, block_size, block_table,
+                       max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                       head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream, k_new, v_new,
+                       kv_new_stride_seq);
 }
 
 // Decode over fp8 (E4M3) pools written by pa_store_kvcache_fp8: the same

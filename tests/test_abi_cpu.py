@@ -116,6 +116,23 @@ def test_decode_host_checks(lib):
     assert call(q=FAKE + 2) == 1   # q must be 16-byte aligned
 
 
+def test_store_decode_host_checks(lib):
+    f = lib.pa_store_decode_paged
+
+    def call(q=FAKE, qs=2048, kn=FAKE, vn=FAKE, ks=1024, kc=FAKE, vc=FAKE, nb=4, bs=16, bt=FAKE, mb=2, ctx=FAKE,
+             ns=2, mctx=32, hq=16, hkv=8, d=128, out=FAKE):
+        return f(q, qs, kn, vn, ks, kc, vc, nb, bs, bt, mb, ctx, ns, mctx, hq, hkv, d, ctypes.c_float(0.1), out,
+                 None, 0, None, None)
+
+    assert call(kn=None) == 1
+    assert call(vn=None) == 1
+    assert call(kn=FAKE + 8) == 1  # k_new must be 16-byte aligned
+    assert call(ks=1000) == 1      # stride below Hkv * D
+    assert call(ks=1028) == 1      # stride not a multiple of 8
+    assert call(d=256, ks=2048) == 2  # then the decode checks apply
+    assert call(ns=0) == 0
+
+
 def test_decode_workspace_follows_the_split_plan(lib):
     """The decode workspace holds fp32 partials [seqs, splits, heads, 128] (256-byte aligned) and a (max, sum)
     pair per (seq, split, head); the keys are split for about 64 CTAs per SM (152 SMs, the GB300 count the

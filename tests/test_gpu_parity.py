@@ -289,6 +289,78 @@ def test_decode_shapes(hq, hkv, bs):
     _decode_vs_oracle(batch)
 
 
+def _store_decode_fused(q, k_new, v_new, kc, vc, tables, ctx, scale, status, max_ctx=None):
+    d = kc.device
+    b = q.shape[0]
+    max_ctx = int(np.max(ctx)) if max_ctx is None else max_ctx
+    ws = torch.empty(max(pa().pa_decode_workspace_bytes(b, q.shape[1], 128, max_ctx), 256), dtype=torch.uint8,
+                     device=d)
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=d)
+    pa().pa_store_decode_paged(q, k_new, v_new, kc, vc, i32(tables, d), i32(ctx, d), max_ctx, scale, out, ws,
+                               dev_status=status.t)
+    return out
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 256), (16, 8, 16), (8, 1, 64), (32, 4, 128), (4, 2, 256)])
+def test_store_decode_fused_equals_store_then_decode(hq, hkv, bs):
+    """pa_store_decode_paged: the same output bits and the same pools (every row) as pa_store_kvcache at the
+    decode step's slots followed by pa_decode_paged."""
+    if (hq, hkv, bs) == (16, 8, 256):
+        batch = wl.decode_batch(device=dev())
+    else:
+        ctx = np.array([1, 15, 16, 17, 255, 256, 257, 1000, 33])
+        batch = wl.paged_batch(700 + hq + bs, ctx, np.ones_like(ctx), bs, num_heads=hq, num_kv_heads=hkv,
+                               device=dev())
+    d = dev()
+    kc1, vc1 = batch.k_cache.clone(), batch.v_cache.clone()
+    st1 = Status(d)
+    gpu_store(batch, kc1, vc1, st1)
+    ref = gpu_decode(batch.tokens.q, kc1, vc1, batch.block_tables, batch.context_lens, batch.scale, st1)
+    kc2, vc2 = batch.k_cache.clone(), batch.v_cache.clone()
+    st2 = Status(d)
+    out = _store_decode_fused(batch.tokens.q, batch.tokens.k, batch.tokens.v, kc2, vc2, batch.block_tables,
+                              batch.context_lens, batch.scale, st2)
+    assert st1.value() == 0 and st2.value() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), "fused output differs"
+    assert torch.equal(kc2.view(torch.int16), kc1.view(torch.int16)), "fused K pool differs"
+    assert torch.equal(vc2.view(torch.int16), vc1.view(torch.int16)), "fused V pool differs"
+
+
+def test_store_decode_fused_padding_rows_and_bad_block():
+    """Padded sequences (context 0) are neither written nor read; a new-token row whose block id is invalid is
+    reported (PA_ERR_BOUNDS) and not written."""
+    d = dev()
+    ctx = np.array([0, 40, 0, 7])
+    batch = wl.paged_batch(602, ctx, np.minimum(ctx, 1), 16, device=d, table_width=4)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    q = torch.randn((4, 16, 128), generator=gen).to(torch.bfloat16).to(d)
+    k_new = torch.randn((4, 8, 128), generator=gen).to(torch.bfloat16).to(d)
+    v_new = torch.randn((4, 8, 128), generator=gen).to(torch.bfloat16).to(d)
+    slots = np.array([-1 if c == 0 else batch.layout.slots(b, [c - 1])[0] for b, c in enumerate(ctx)], np.int32)
+    kc1, vc1 = batch.k_cache.clone(), batch.v_cache.clone()
+    st1 = Status(d)
+    pa().pa_store_kvcache(k_new, v_new, kc1, vc1, i32(slots, d), dev_status=st1.t)
+    ref = gpu_decode(q, kc1, vc1, batch.block_tables, ctx, batch.scale, st1)
+    kc2, vc2 = batch.k_cache.clone(), batch.v_cache.clone()
+    st2 = Status(d)
+    out = _store_decode_fused(q, k_new, v_new, kc2, vc2, batch.block_tables, ctx, batch.scale, st2)
+    assert st1.value() == 0 and st2.value() == 0
+    assert (out[0] == 0).all() and (out[2] == 0).all()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(kc2.view(torch.int16), kc1.view(torch.int16))
+    assert torch.equal(vc2.view(torch.int16), vc1.view(torch.int16))
+    # sequence 3's new token (position 6) lives in table entry 0: make it invalid
+    bad = batch.block_tables.copy()
+    bad[3, 0] = -1
+    kc3, vc3 = batch.k_cache.clone(), batch.v_cache.clone()
+    st3 = Status(d)
+    _store_decode_fused(q, k_new, v_new, kc3, vc3, bad, ctx, batch.scale, st3)
+    assert st3.value() == 4
+    row3 = slots[3]
+    assert torch.equal(kc3.view(-1, 8, 128)[row3].view(torch.int16),
+                       batch.k_cache.view(-1, 8, 128)[row3].view(torch.int16)), "row with a bad block id was written"
+
+
 def test_decode_padded_rows_and_bounds():
     d = dev()
     ctx = np.array([0, 40, 0, 7])
