@@ -52,8 +52,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 # DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
 # valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha256": "de5643ab3809b566bd2d818eff1c6470ba994e5120f1bbb3acd9089501d2fde5",
-               "bytes_per_call": 587_109_888 + 6_950_912, "kernel": "decode_split_kernel<2, 0>"}
+NCU_TRAFFIC = {"source_sha256": "35b05e8752c91a03b40295e883e21e0b92e6a781586d4fb54e15d012c7c85fec",
+               "bytes_per_call": 587_302_912 + 7_577_344, "kernel": "decode_split_kernel<2, 0>"}
 
 
 def _file_sha(path):
