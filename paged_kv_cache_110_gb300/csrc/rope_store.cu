@@ -97,7 +97,8 @@ __device__ __forceinline__ void norm_rope_pairs(uint2 &lo, uint2 &hi, const uint
 // cos / sin row into a ring of STAGES shared-memory stages with bulk copies,
 // several tokens ahead, so the bytes in flight do not depend on registers;
 // warps 0-3 take the rows of the token in the front stage, a half-warp per
-// 256-byte row, and write Q, K and V out with 16-byte stores.
+// 256-byte row, and write Q and K out as two 8-byte pieces per lane (a lane's
+// rotation pairs) and V rows with 16-byte stores.
 constexpr int STAGES = 4;
 constexpr int COMPUTE_WARPS = 4;
 constexpr int RS_THREADS = (COMPUTE_WARPS + 1) * 32;
