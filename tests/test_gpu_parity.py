@@ -95,6 +95,32 @@ def test_prefill_varlen_16k():
     _prefill_case(wl.varlen_prefill(device=dev()))
 
 
+def test_prefill_causal_rows_ignore_the_future():
+    """Changing the last 40 tokens of every sequence (their q, k and v) leaves every earlier row's output
+    bit-identical: a masked key gets -inf before the row maximum and contributes exactly 0 (the pages' causal-mask
+    check, here on the CUDA path)."""
+    d = dev()
+    batch = wl.varlen_prefill(device=d)
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    st = Status(d)
+    gpu_store(batch, kc, vc, st)
+    out1 = gpu_prefill(batch, kc, vc, paged=True, status=st)
+    cu = batch.cu_seqlens_q
+    late = np.concatenate([np.arange(max(cu[b], cu[b + 1] - 40), cu[b + 1]) for b in range(len(cu) - 1)])
+    late_t = torch.as_tensor(late, device=d)
+    gen = torch.Generator(device="cpu").manual_seed(9)
+    qkv = batch.tokens.qkv
+    qkv[late_t] = (torch.randn((len(late), qkv.shape[1]), generator=gen) * 3).to(torch.bfloat16).to(d)
+    kc2, vc2 = batch.k_cache.clone(), batch.v_cache.clone()
+    gpu_store(batch, kc2, vc2, st)
+    out2 = gpu_prefill(batch, kc2, vc2, paged=True, status=st)
+    assert st.value() == 0
+    early = np.setdiff1d(np.arange(int(cu[-1])), late)
+    early_t = torch.as_tensor(early, device=d)
+    assert torch.equal(out1[early_t].view(torch.int16), out2[early_t].view(torch.int16))
+    assert not torch.equal(out1[late_t].view(torch.int16), out2[late_t].view(torch.int16))
+
+
 def test_prefill_out_aligned_to_16_bytes_only():
     """An output buffer that starts 16 bytes past a 32-byte boundary (allowed:
     the entry point asks for 16) takes the 16-byte-store epilogue instead of
