@@ -4,17 +4,22 @@ A step is one decode step of the decode-batch workload through all 28 layers:
 for each layer, the KV write of the 256 new tokens into that layer's pool and
 paged decode attention of the 256 queries (256 sequences, context_lens
 U[100, 1024], block_size 256, 16 query / 8 KV heads x 128, bf16; every layer
-has its own pool, so the 28 pools, about 20 GB, never fit in L2).
+has its own pool, so the 28 pools, about 20 GB, never fit in L2).  Each layer
+is one pa_store_decode_paged call (the KV write fused into the decode launch);
+the step is captured once in a CUDA graph and replayed.
 
 The JSON line reports:
   value         algorithmic HBM bytes of the step (KV write + decode) / step
                 time, GB/s, device-resident inputs, CUDA events;
   tokens_per_s  decode tokens per second (256 per step);
+  eager         the same calls launched one by one from Python;
+  unfused       the same step with pa_store_kvcache + pa_decode_paged per
+                layer, also graph-captured;
   e2e           the same metric through the C ABI with inputs copied from
                 pinned host memory and outputs copied back inside the timed
                 region;
-  roofline      of the decode call (split + merge kernels), against the
-                measured HBM copy bandwidth;
+  roofline      of the fused KV write + decode call (split kernel and merge),
+                against the measured HBM copy bandwidth;
   prefill       the varlen-prefill (16384 packed tokens) and prefix+chunk
                 workloads: KV write + prefill, TFLOP/s of visible pairs;
   long_decode   the 512-sequence, 4096-context decode, GB/s;
