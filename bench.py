@@ -402,6 +402,12 @@ def flush_l2(buf):
     buf[half:].max()
 
 
+def prefill_ws(pa, num_seqs, max_q, max_k, device):
+    """The caller-owned workspace a prefill call asks for (at least 256 bytes)."""
+    n = pa.pa_prefill_workspace_bytes(num_seqs, int(max_q), int(max_k), HQ, HKV)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
 def time_prefill(device, steps, warmup, flush, only="all"):
     from paged_kv_cache_110_gb300 import binding as pa
     res = {}
@@ -574,9 +580,11 @@ def time_block_size_sweep(device, steps, warmup, flush):
             pbt = torch.as_tensor(p.block_tables, device=device)
             cq, ck = (torch.as_tensor(x, device=device) for x in (p.cu_seqlens_q, p.cu_seqlens_k))
 
+            pws = prefill_ws(pa, p.layout.num_seqs, int(lens.max()), int(lens.max()), device)
+
             def pre():
                 pa.pa_prefill_paged(p.tokens.q, cq, ck, int(lens.max()), int(lens.max()), p.scale, pout,
-                                    k_cache=p.k_cache, v_cache=p.v_cache, block_table=pbt)
+                                    k_cache=p.k_cache, v_cache=p.v_cache, block_table=pbt, workspace=pws)
 
             for _ in range(warmup):
                 pre()
@@ -666,12 +674,16 @@ def time_mixed(device, steps, warmup, flush):
     ws = torch.empty(max(pa.pa_decode_workspace_bytes(256, HQ, D, max_d), 256), dtype=torch.uint8, device=device)
     outd = torch.empty((256, HQ, D), dtype=torch.bfloat16, device=device)
 
+    ws_mixed = prefill_ws(pa, len(ctx), 512, int(ctx.max()), device)
+    ws_chunk = prefill_ws(pa, 1, 512, 2560, device)
+
     def mixed():
         pa.pa_prefill_paged(b.tokens.q, cq, ck, 512, int(ctx.max()), b.scale, out, k_cache=kc, v_cache=vc,
-                            block_table=bt)
+                            block_table=bt, workspace=ws_mixed)
 
     def separate():
-        pa.pa_prefill_paged(q1, cq1, ck1, 512, 2560, b.scale, out1, k_cache=kc, v_cache=vc, block_table=bt[:1])
+        pa.pa_prefill_paged(q1, cq1, ck1, 512, 2560, b.scale, out1, k_cache=kc, v_cache=vc, block_table=bt[:1],
+                            workspace=ws_chunk)
         pa.pa_decode_paged(qd, kc, vc, bt[1:], ctx_d, max_d, b.scale, outd, ws)
 
     res = {}

@@ -353,8 +353,11 @@ pa_status pa_decode_paged_fp8(const void *q, int64_t q_stride_seq, const void *k
  *     max_context_len) exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES, it returns
  *     PA_ERR_UNSUPPORTED and launches nothing; use pa_decode_paged then.
  *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture begins.
+ *     (with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture begins.  After
+ *     cudaDeviceReset (or any reset of the device's primary context) the
+ *     library's module is loaded again at another address and the kept one
+ *     is stale: do not call this entry point after such a reset.
  *   - All calls share the one array: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and give wrong
  *     results.  Calls on one stream are ordered and safe.  The array keeps

@@ -280,8 +280,9 @@ def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
                      k_cache=None, v_cache=None, block_table=None, workspace=None, dev_status=None, stream=None):
     """Causal varlen prefill.  With block_table=None keys come from k/v;
     otherwise from the paged caches.  workspace: a CUDA uint8 tensor of at
-    least pa_prefill_workspace_bytes(...) bytes; when None and one is needed,
-    it is allocated here (through PyTorch's allocator)."""
+    least pa_prefill_workspace_bytes(...) bytes (256-byte aligned), owned by
+    the caller; nothing is allocated here, and a call that needs a workspace
+    and gets none raises."""
     hq, qs = _bf16_rows(q, "q")
     if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (q.shape[0], hq, q.shape[2]):
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
@@ -304,11 +305,13 @@ def pa_prefill_paged(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
             raise ValueError("block_table must be [num_seqs, max_blocks]")
         args = (None, None, 0, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_table), block_table.shape[1])
     need = lib.pa_prefill_workspace_bytes(nseq, int(max_seqlen_q), int(max_seqlen_k), hq, hkv) if nseq > 0 else 0
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        raise ValueError(f"pa_prefill_paged: this call needs a workspace of {need} bytes "
+                         "(pa_prefill_workspace_bytes)")
     _check(lib.pa_prefill_paged(_ptr(q), qs, q.shape[0], *args, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
                                 int(max_seqlen_q), int(max_seqlen_k), hq, hkv, q.shape[2], float(scale), _ptr(out),
-                                _ptr(workspace), 0 if workspace is None else workspace.numel(), _ptr(dev_status),
+                                _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _ptr(dev_status),
                                 _stream(stream)),
            "pa_prefill_paged")
 

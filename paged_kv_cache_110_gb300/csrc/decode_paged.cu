@@ -30,7 +30,6 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -81,20 +80,17 @@ Plan make_plan(int num_seqs, int max_ctx)
 {
     Plan p{CHUNK, 0};
     if (num_seqs <= 0 || max_ctx <= 0) return p;
-    int split = 0;
-    if (const char *env = std::getenv("PA_DECODE_SPLIT_TOKENS")) split = std::atoi(env);
-    if (split <= 0) {
-        // Many CTAs keep enough loads in flight (about 64 per SM measured best for
-        // long contexts), but a split shorter than 128 tokens costs more in
-        // fixed work and partials than it gains (measured on 1k contexts).
-        const int sms = pa::num_sms() > 0 ? pa::num_sms() : 152;
-        const long long target_ctas = 64LL * sms;
-        long long per_seq = (target_ctas + num_seqs - 1) / num_seqs;
-        if (per_seq < 1) per_seq = 1;
-        long long len = (max_ctx + per_seq - 1) / per_seq;
-        len = (len + 63) / 64 * 64;
-        split = int(len < 128 ? 128 : len);
-    }
+    // Many CTAs keep enough loads in flight (about 64 per SM measured best for
+    // long contexts), but a split shorter than 128 tokens costs more in
+    // fixed work and partials than it gains (measured on 1k contexts).  The
+    // plan depends only on the call's arguments and the device's SM count.
+    const int sms = pa::num_sms() > 0 ? pa::num_sms() : 152;
+    const long long target_ctas = 64LL * sms;
+    long long per_seq = (target_ctas + num_seqs - 1) / num_seqs;
+    if (per_seq < 1) per_seq = 1;
+    long long len = (max_ctx + per_seq - 1) / per_seq;
+    len = (len + 63) / 64 * 64;
+    int split = int(len < 128 ? 128 : len);
     split = (split + CHUNK - 1) / CHUNK * CHUNK;
     p.split_len = split;
     p.max_splits = (max_ctx + split - 1) / split;
@@ -737,7 +733,8 @@ extern "C" pa_status pa_decode_paged_noalloc(const void *q, int64_t q_stride_seq
                                              int num_heads, int num_kv_heads, int head_dim, float scale, void *out,
                                              int32_t *dev_status, void *stream)
 {
-    if (num_seqs < 0 || max_context_len < 0 || num_heads <= 0 || head_dim != D) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || max_context_len < 0 || num_heads <= 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != D) return PA_ERR_UNSUPPORTED;
     if (pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len) > PA_DECODE_NOALLOC_SCRATCH_BYTES)
         return PA_ERR_UNSUPPORTED;
     void *scratch = nullptr;

@@ -1,5 +1,7 @@
 // pa_api.cu -- status strings, sizes and device queries of libpa.
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "pa_common.cuh"
 
@@ -18,6 +20,21 @@ int num_sms()
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes)
+{
+    // the attribute belongs to the device current at the time of the call
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev}) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({kernel, dev});
+    return e;
 }
 
 pa_status launch_status()

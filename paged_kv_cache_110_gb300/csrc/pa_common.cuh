@@ -79,6 +79,11 @@ inline bool pow2_in(int x, int lo, int hi)
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// Let `kernel` use `bytes` of dynamic shared memory on the current device (an
+// opt-in each device needs once; cached per device and kernel).  Callers pass
+// the largest size any launch of that kernel uses.
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
+
 // PA_OK if cudaGetLastError() is clean, else PA_ERR_CUDA.
 pa_status launch_status();
 

@@ -1000,16 +1000,9 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
             !make_rows_map(&p.vmap, v, num_tokens, num_kv_heads, kv_stride_tok, BN))
             return PA_ERR_CUDA;
     }
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
+    if (pa::allow_dynamic_smem(reinterpret_cast<const void *>(prefill_tc_kernel<false>), SMEM_BYTES) != cudaSuccess ||
+        pa::allow_dynamic_smem(reinterpret_cast<const void *>(prefill_tc_kernel<true>), SMEM_BYTES) != cudaSuccess)
+        return PA_ERR_CUDA;
     const int64_t units = pl.items * pl.kv_splits;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
     const dim3 grid(unsigned(units < sms ? units : sms));

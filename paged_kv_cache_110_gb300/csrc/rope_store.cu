@@ -350,14 +350,10 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     // 16 query and 8 KV heads)
     const int rows = num_heads + 2 * num_kv_heads;
     const size_t smem = size_t(STAGES) * stage_bytes(rows) + 2 * STAGES * 8 + 16;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        // the largest QKV row: 64 query heads and 8 KV heads
-        const size_t most = size_t(STAGES) * stage_bytes(64 + 2 * 8) + 2 * STAGES * 8 + 16;
-        attr_err = cudaFuncSetAttribute(norm_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(most));
-    });
-    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
+    // the largest QKV row: 64 query heads and 8 KV heads
+    const size_t most = size_t(STAGES) * stage_bytes(64 + 2 * 8) + 2 * STAGES * 8 + 16;
+    if (pa::allow_dynamic_smem(reinterpret_cast<const void *>(norm_rope_store_kernel), int(most)) != cudaSuccess)
+        return PA_ERR_CUDA;
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 148;
     const int64_t cap = int64_t(sms) * 6;
     const unsigned grid = unsigned(num_tokens < cap ? num_tokens : cap);

@@ -57,14 +57,21 @@ def oracle_store(batch, kc_bits, vc_bits, tokens=None, slots=None):
     assert rc == oracle.OK
 
 
+def prefill_workspace(num_seqs, max_q, max_k, hq, hkv, device):
+    """The caller-owned workspace a prefill call asks for (None if it needs none)."""
+    n = pa().pa_prefill_workspace_bytes(num_seqs, int(max_q), int(max_k), hq, hkv)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
 def gpu_prefill(batch, kc, vc, paged=True, status=None, tokens=None):
     d = kc.device
     toks = batch.tokens if tokens is None else tokens
     out = torch.empty(toks.q.shape, dtype=torch.bfloat16, device=d)
     kw = dict(k_cache=kc, v_cache=vc, block_table=i32(batch.block_tables, d)) if paged else dict(k=toks.k, v=toks.v)
-    pa().pa_prefill_paged(toks.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d),
-                          int(batch.query_lens.max()), int(batch.context_lens.max()), batch.scale, out,
-                          dev_status=None if status is None else status.t, **kw)
+    max_q, max_k = int(batch.query_lens.max()), int(batch.context_lens.max())
+    ws = prefill_workspace(len(batch.cu_seqlens_q) - 1, max_q, max_k, toks.q.shape[1], kc.shape[2], d)
+    pa().pa_prefill_paged(toks.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d), max_q, max_k,
+                          batch.scale, out, workspace=ws, dev_status=None if status is None else status.t, **kw)
     return out
 
 

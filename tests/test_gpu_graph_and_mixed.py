@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import MAX_ABS, MEAN_ABS, Status, assert_close, dev, i32, oracle_prefill, oracle_store, pa
+from gpu_helpers import (MAX_ABS, MEAN_ABS, Status, assert_close, dev, i32, oracle_prefill, oracle_store, pa,
+                         prefill_workspace)
 from paged_kv_cache_110_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -127,9 +128,10 @@ def test_mixed_decode_rows_and_prefill_chunks_in_one_launch():
     pa().pa_store_kvcache(batch.tokens.k, batch.tokens.v, kc, vc, i32(batch.slot_mapping, d))
     out = torch.empty(batch.tokens.q.shape, dtype=torch.bfloat16, device=d)
     st = Status(d)
+    ws = prefill_workspace(len(ctx), int(ql.max()), int(ctx.max()), 16, 8, d)
     pa().pa_prefill_paged(batch.tokens.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d), int(ql.max()),
                           int(ctx.max()), batch.scale, out, k_cache=kc, v_cache=vc,
-                          block_table=i32(batch.block_tables, d), dev_status=st.t)
+                          block_table=i32(batch.block_tables, d), workspace=ws, dev_status=st.t)
     torch.cuda.synchronize()
     assert int(st.t.item()) == 0
     oracle_store(batch, kc_bits, vc_bits)

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from gpu_helpers import (MAX_ABS, MEAN_ABS, Status, assert_close, compact_pool, dev, gpu_decode, gpu_prefill, gpu_store, i32,
-                         oracle_prefill, oracle_store, pa)
+                         oracle_prefill, oracle_store, pa, prefill_workspace)
 from oracle_cases import bits
 from paged_kv_cache_110_gb300 import workloads as wl
 
@@ -135,9 +135,11 @@ def test_prefill_out_aligned_to_16_bytes_only():
     out = buf[8:8 + n].view(ref.shape)  # 8 bf16 = 16 bytes in
     assert out.data_ptr() % 32 == 16
     d = kc.device
-    pa().pa_prefill_paged(batch.tokens.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d),
-                          int(batch.query_lens.max()), int(batch.context_lens.max()), batch.scale, out,
-                          dev_status=st.t, k_cache=kc, v_cache=vc, block_table=i32(batch.block_tables, d))
+    max_q, max_k = int(batch.query_lens.max()), int(batch.context_lens.max())
+    ws = prefill_workspace(batch.layout.num_seqs, max_q, max_k, 16, 8, d)
+    pa().pa_prefill_paged(batch.tokens.q, i32(batch.cu_seqlens_q, d), i32(batch.cu_seqlens_k, d), max_q, max_k,
+                          batch.scale, out, workspace=ws, dev_status=st.t, k_cache=kc, v_cache=vc,
+                          block_table=i32(batch.block_tables, d))
     assert st.value() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all()
@@ -184,7 +186,10 @@ def test_prefix_cache_and_chunked_prefill():
     oracle_store(a, kb, vb)
     oracle_store(b, kb, vb)
     np.testing.assert_array_equal(wl.bf16_bits(kc), kb)
-    seqs = [0, 1, 17, 31]
+    # eight of call A's 32 sequences or more: both ends, a spread between, and
+    # the longest and shortest suffixes
+    ql = a.query_lens
+    seqs = sorted({0, 1, 5, 11, 17, 23, 30, 31, int(np.argmax(ql)), int(np.argmin(ql))})
     ref_a, rows_a = oracle_prefill(a, kb, vb, seqs=seqs)
     assert_close(out_a[torch.as_tensor(rows_a, device=out_a.device)], ref_a, "prefix call a")
     ref_b, _ = oracle_prefill(b, kb, vb)
@@ -243,7 +248,8 @@ def test_worked_example_through_gpu():
     q = torch.as_tensor(x, dtype=torch.bfloat16, device=d)
     out = torch.empty_like(q)
     cu = i32([0, 3], d)
-    pa().pa_prefill_paged(q, cu, cu, 3, 3, 1 / math.sqrt(2), out, k=q, v=q)
+    pa().pa_prefill_paged(q, cu, cu, 3, 3, 1 / math.sqrt(2), out, k=q, v=q,
+                          workspace=prefill_workspace(1, 3, 3, 1, 1, d))
     got = out[:, 0, :2].double().cpu().numpy()
     np.testing.assert_allclose(got[-1], [0.7517, 0.7517], atol=1e-2)
     np.testing.assert_allclose(got[1], [0.3302, 0.6698], atol=1e-2)
@@ -301,7 +307,9 @@ def test_decode_batch_256():
 
 def test_decode_long_context_512_full_size_sampled():
     batch = wl.long_decode(device=dev())
-    seqs = [0, 1, 2, 100, 255, 256, 400, 511]
+    ctx = batch.context_lens
+    seqs = sorted({0, 1, 2, 37, 100, 128, 200, 255, 256, 301, 384, 400, 450, 500, 510, 511,
+                   int(np.argmax(ctx)), int(np.argmin(ctx))})
     out, _, _ = _decode_vs_oracle(batch, seqs=seqs)
     assert torch.isfinite(out.float()).all()
 
@@ -350,6 +358,36 @@ def test_store_decode_fused_equals_store_then_decode(hq, hkv, bs):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), "fused output differs"
     assert torch.equal(kc2.view(torch.int16), kc1.view(torch.int16)), "fused K pool differs"
     assert torch.equal(vc2.view(torch.int16), vc1.view(torch.int16)), "fused V pool differs"
+
+
+def test_store_decode_fused_decode_batch_vs_oracle():
+    """pa_store_decode_paged on the decode-batch workload (256 sequences, block size 256), in the launch
+    configuration the step uses, against the oracle's KV write + decode on a sample of sequences.  The oracle's
+    write slots come from its own decode metadata builder (position context_lens[b] - 1 through the table), not
+    from the input generator; the written pool rows are compared too."""
+    d = dev()
+    batch = wl.decode_batch(device=d)
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    st = Status(d)
+    out = _store_decode_fused(batch.tokens.q, batch.tokens.k, batch.tokens.v, kc, vc, batch.block_tables,
+                              batch.context_lens, batch.scale, st)
+    assert st.value() == 0
+    ctx = batch.context_lens
+    seqs = sorted({0, 1, 2, 31, 63, 64, 100, 127, 128, 180, 200, 233, 254, 255,
+                   int(np.argmax(ctx)), int(np.argmin(ctx))})
+    bs = batch.layout.block_size
+    kb, vb, tables = compact_pool(batch.block_tables, ctx, seqs, batch.k_cache, batch.v_cache, bs)
+    meta, rc = oracle.prepare_decode(ctx[seqs], tables, bs, kb.shape[0])
+    assert rc == oracle.OK
+    np.testing.assert_array_equal(meta["context_lens"], ctx[seqs])
+    rc = oracle.store_kvcache(wl.bf16_bits(batch.tokens.k)[seqs], wl.bf16_bits(batch.tokens.v)[seqs], kb, vb,
+                              meta["slot_mapping"])
+    assert rc == oracle.OK
+    ref = oracle.decode(wl.bf16_bits(batch.tokens.q)[seqs], kb, vb, tables, meta["context_lens"], batch.scale)
+    assert_close(out[torch.as_tensor(seqs, device=d)], ref, "fused KV write + decode, decode batch")
+    kg, vg, _ = compact_pool(batch.block_tables, ctx, seqs, kc, vc, bs)
+    np.testing.assert_array_equal(kg, kb)
+    np.testing.assert_array_equal(vg, vb)
 
 
 def test_store_decode_fused_padding_rows_and_bad_block():

@@ -5,14 +5,18 @@ manager).  Its scratch is a fixed device array inside the library, so it
 takes no workspace.
 
 Checked through the C ABI against pa_decode_paged (which takes a caller
-workspace) on two calls in a row with different inputs, within the attention
-tolerance the other GPU tests use; and sizes beyond the fixed scratch are
-refused without a launch.  This file is collected last on purpose.
+workspace) on two calls in a row with different inputs: both run the same
+plan and kernels, so the outputs must be identical bit for bit.  The second
+batch (mixed lengths, partly single-split, partly multi-split) is also
+compared with the CPU oracle within the attention tolerance the other GPU
+tests use; and sizes beyond the fixed scratch are refused without a launch.
+This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_110_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -58,9 +62,18 @@ def test_noalloc_matches_workspace_decode_on_two_calls(pa):
                             device=d)
     for batch in (first, second):
         got, ref = _decode_both(pa, batch)
-        err = (got.double() - ref.double()).abs()
         assert torch.isfinite(got.float()).all()
-        assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    # the second call against the oracle (history rows plus the new token
+    # written by the oracle's own KV write)
+    kb, vb = wl.bf16_bits(second.k_cache).copy(), wl.bf16_bits(second.v_cache).copy()
+    rc = oracle.store_kvcache(wl.bf16_bits(second.tokens.k), wl.bf16_bits(second.tokens.v), kb, vb,
+                              second.slot_mapping)
+    assert rc == oracle.OK
+    want = oracle.decode(wl.bf16_bits(second.tokens.q), kb, vb, second.block_tables, second.context_lens,
+                         second.scale)
+    err = np.abs(got.double().cpu().numpy() - want)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(pa):
