@@ -241,6 +241,20 @@ pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64_t num_toke
                            int32_t *dev_status, void *stream);
 
 /*
+ * Test hook, not part of the computation: makes the bounded waits of
+ * pa_prefill_paged and pa_norm_rope_store_kvcache run out, for the calls
+ * launched after this one (process-wide).  With cycles > 0, one wait of every
+ * CTA of those kernels (the prefill's MMA issuer, the fused write's compute
+ * warps) is on a barrier that nothing arrives on, and every pipeline wait
+ * gives up after `cycles` SM clock cycles instead of the default 2^31 (about a
+ * second).  0 restores normal operation.  A call whose wait gives up writes
+ * PA_ERR_TIMEOUT to *dev_status; its CTAs then wait for their own copies and
+ * MMAs in flight (those waits keep the default limit), free their tensor
+ * memory and return, leaving the output incomplete and the stream usable.
+ */
+void pa_test_stall_pipelines(long long cycles);
+
+/*
  * Bytes of scratch pa_decode_paged needs for these host-side sizes on the
  * current device (it depends on the device's SM count).  Returns 0 when the
  * arguments are invalid.

@@ -20,7 +20,7 @@ __all__ = [
     "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_norm_rope_store_kvcache", "pa_rope_cos_sin_table",
     "pa_prepare_prefill", "pa_prepare_decode", "pa_prefill_workspace_bytes", "pa_prefill_paged",
     "pa_decode_workspace_bytes", "pa_decode_paged", "pa_store_decode_paged", "pa_decode_paged_fp8",
-    "pa_decode_paged_noalloc",
+    "pa_decode_paged_noalloc", "pa_test_stall_pipelines",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
@@ -73,6 +73,8 @@ def _load() -> ctypes.CDLL:
     L.pa_store_decode_paged.restype = i32
     L.pa_store_decode_paged.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                         f32, vp, vp, sz, vp, vp]
+    L.pa_test_stall_pipelines.restype = None
+    L.pa_test_stall_pipelines.argtypes = [ctypes.c_longlong]
     L.pa_decode_paged_noalloc.restype = i32
     L.pa_decode_paged_noalloc.argtypes = [vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32, f32,
                                           vp, vp, vp]
@@ -92,6 +94,13 @@ def pa_abi_version() -> int:
 
 def pa_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
     return lib.pa_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes)
+
+
+def pa_test_stall_pipelines(cycles: int) -> None:
+    """Test hook: later prefill and fused norm + RoPE + KV write calls stall on
+    a barrier nothing arrives on and give up after `cycles` SM cycles
+    (PA_ERR_TIMEOUT); 0 restores normal operation."""
+    lib.pa_test_stall_pipelines(int(cycles))
 
 
 # ---------------------------------------------------------------- marshalling helpers

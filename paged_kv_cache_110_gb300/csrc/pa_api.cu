@@ -1,4 +1,5 @@
 // pa_api.cu -- status strings, sizes and device queries of libpa.
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -37,6 +38,18 @@ cudaError_t allow_dynamic_smem(const void *kernel, int bytes)
     return e;
 }
 
+namespace {
+std::atomic<long long> g_test_wait_limit{0};
+}
+
+long long pipeline_wait_limit(long long dflt)
+{
+    const long long v = g_test_wait_limit.load(std::memory_order_relaxed);
+    return v > 0 ? v : dflt;
+}
+
+bool pipeline_test_stall() { return g_test_wait_limit.load(std::memory_order_relaxed) > 0; }
+
 pa_status launch_status()
 {
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -58,6 +71,11 @@ extern "C" const char *pa_status_string(int status)
 }
 
 extern "C" int pa_abi_version(void) { return 100; }
+
+extern "C" void pa_test_stall_pipelines(long long cycles)
+{
+    pa::g_test_wait_limit.store(cycles > 0 ? cycles : 0, std::memory_order_relaxed);
+}
 
 extern "C" size_t pa_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int elem_bytes)
 {

@@ -84,6 +84,12 @@ int num_sms();
 // the largest size any launch of that kernel uses.
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
 
+// The limit, in SM cycles, of the waits inside a kernel's pipeline: `dflt`,
+// unless a test set another with pa_test_stall_pipelines; and whether such a
+// test asked one wait per CTA to be on a barrier nothing arrives on.
+long long pipeline_wait_limit(long long dflt);
+bool pipeline_test_stall();
+
 // PA_OK if cudaGetLastError() is clean, else PA_ERR_CUDA.
 pa_status launch_status();
 

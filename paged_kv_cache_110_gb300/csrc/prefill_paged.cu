@@ -9,16 +9,18 @@
 // reads KV head h / (Hq / Hkv) (§19.6).  Softmax is accumulated blockwise with
 // a running max, a running sum and an unnormalised numerator (§13.3).
 //
-// A persistent kernel: one CTA per SM takes work items from a device counter,
-// heaviest first.  An item is a PAIR of 128-row query tiles that read the same
+// A persistent kernel: one CTA per SM; the valid work items, heaviest first,
+// are dealt to the CTAs statically in snake order (CTA c of C takes the
+// valid items of rank c, 2C - 1 - c, 2C + c, ...), so that no counter in
+// device memory is needed: every CTA ranks the items itself, 32 at a time.  An item is a PAIR of 128-row query tiles that read the same
 // keys: the same rows of two query heads of one KV group (GQA), or, when every
 // KV head has a single query head, two consecutive row tiles of one head.
 // Each K and V tile is loaded once for both, and while one tile's softmax runs
 // the tensor cores work on the other's, so the two dependency chains
 // (S -> softmax -> P.V) hide each other.
-//   warp 3      scheduler: fetches items, decodes each once and publishes it
-//               in a ring of 4, stages its block ids (validated) and loads its
-//               two Q tiles by TMA into two Q buffers.
+//   warp 3      scheduler: walks this CTA's items, decodes each once and
+//               publishes it in a ring of 4, stages its block ids (validated)
+//               and loads its two Q tiles by TMA into two Q buffers.
 //   warp 0      K producer, warp 2 V producer: paged tiles arrive by TMA, one
 //               box per page run (box height gcd(block_size, 128) rows, so a
 //               box never crosses a page); without a table one box of 128
@@ -44,7 +46,7 @@
 //               rescaled in TMEM; O / l uses the same max, so the result is
 //               exact.  Epilogue: O / l to bf16, one row per thread.
 // Every wait is bounded: on a timeout the CTA records PA_ERR_TIMEOUT, drains
-// what it issued, frees its TMEM and exits.
+// what it issued (TMA loads of Q, K and V, and MMAs), frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -92,7 +94,8 @@ enum {
     B_IRF = B_TE + 2,            // item-ring slot published (1 arrival)
     B_IRE = B_IRF + RING,        // item-ring slot read by every role (11 arrivals)
     B_DRAIN = B_IRE + RING,
-    NBAR = B_DRAIN + 1
+    B_STALL = B_DRAIN + 1,       // never arrived on: the wait a test makes run out
+    NBAR = B_STALL + 1
 };
 constexpr int IR_READERS = 2 + 1 + 8;             // producer warps, MMA warp, softmax warps
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM address, abort flag
@@ -134,19 +137,19 @@ struct TcParams {
     uint16_t *out;
     int out_v8;       // out is 32-byte aligned: the epilogue stores 32 bytes per instruction
     int32_t *status;
-    unsigned int sched_slot;  // which scheduler counter pair this call uses
+    long long wait_limit;     // SM cycles a pipeline wait may take before the call gives up
+    int test_stall;           // test hook: the MMA warp first waits on a barrier nothing arrives on
     int kv_splits;            // key ranges per item (1: no split); split items write partials
     float *ws_o;              // [unit][QT][BM][D] unnormalised O of split items
     float2 *ws_ml;            // [unit][QT][BM] (running max in scaled log2 units, exponent sum)
 };
 
-// Work-item counters, one pair [next item, CTAs finished] per call in flight.
-// Each launch takes the next pair round-robin; they start at zero (static
-// storage) and the last CTA of a launch sets its pair back to zero, so a launch
-// always finds its pair at zero unless SCHED_SLOTS later launches were issued
-// while it still runs on another stream.
-constexpr unsigned SCHED_SLOTS = 4096;
-__device__ unsigned int g_prefill_sched[SCHED_SLOTS][2];
+// The CTA (of C) that takes the valid item of rank r in the snake order.
+__device__ __forceinline__ int owner_of(int r, int nctas)
+{
+    const int round = r / nctas, pos = r % nctas;
+    return (round & 1) ? nctas - 1 - pos : pos;
+}
 
 // Parity of completion number n of a barrier used by every nbuf-th round.
 __device__ __forceinline__ uint32_t par(int n, int nbuf) { return uint32_t(n / nbuf) & 1u; }
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             mbar_init(bar(B_IRE + s), IR_READERS);
         }
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_STALL), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     // releases the slot).  Returns the item number, -1 at the end, -2 on abort.
     auto read_ring = [&](int n, Item &it) -> int {
         const int slot = n % RING;
-        if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) return -2;
+        if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, p.wait_limit))) return -2;
         const int w = ring[slot].w;
         if (w >= 0) it = ring[slot].it;
         __syncwarp();
@@ -378,33 +382,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
     if (warp == 3) {
         // ------------------------------------------------------------ scheduler
-        // Fetch work items from the call's counter (heaviest first), publish each
-        // in the item ring, stage its block ids (validated) for the producers and
-        // load its two Q tiles.
+        // Walk this CTA's items (heaviest first), publish each in the item ring,
+        // stage its block ids (validated) for the producers and load its two Q
+        // tiles.
         if (lane == 0) tma_prefetch_desc(&p.qmap);
-        int n = 0;  // items published
+        int n = 0;      // items published
+        int qdone = 0;  // Q tiles announced (a TMA load, or an arrival for an empty tile)
+        // The items are ranked 32 at a time (a lane each): window `win` of the
+        // item list, `vbase` valid items before it, `mine` this CTA's items of
+        // the window not yet published.
+        int win = 0, vbase = 0;
+        uint32_t mine = 0;
         while (true) {
             int w = -1;
-            while (true) {
-                int cand = 0;
-                if (lane == 0) cand = int(atomicAdd(&g_prefill_sched[p.sched_slot][0], 1u));
-                cand = __shfl_sync(FULL, cand, 0);
-                if (cand >= n_items) break;
-                const Item it = decode_item<SPLIT>(p, cand);
-                if (it.bad && lane == 0) pa::report(p.status, it.bad_code);
-                if (it.valid) {
-                    w = cand;
-                    break;
+            while (mine == 0 && win < n_items) {
+                const int u = win + lane;
+                bool v = false;
+                if (u < n_items) {
+                    const Item it = decode_item<SPLIT>(p, u);
+                    v = it.valid;
+                    if (it.bad) pa::report(p.status, it.bad_code);
                 }
+                const uint32_t vm = __ballot_sync(FULL, v);
+                const int r = vbase + __popc(vm & ((1u << lane) - 1u));
+                mine = __ballot_sync(FULL, v && owner_of(r, int(gridDim.x)) == int(blockIdx.x));
+                vbase += __popc(vm);
+                win += 32;
+            }
+            if (mine != 0) {
+                w = win - 32 + __ffs(mine) - 1;
+                mine &= mine - 1u;
             }
             const int slot = n % RING, tb = n & 1;
             if (n >= RING &&
-                !__all_sync(FULL, mbar_wait(bar(B_IRE + slot), par(n - RING, RING), abort_flag, WAIT_LIMIT)))
+                !__all_sync(FULL, mbar_wait(bar(B_IRE + slot), par(n - RING, RING), abort_flag, p.wait_limit)))
                 break;
             Item it;
             if (w >= 0) {
                 it = decode_item<SPLIT>(p, w);
-                if (n >= 2 && !__all_sync(FULL, mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, WAIT_LIMIT)))
+                if (n >= 2 && !__all_sync(FULL, mbar_wait(bar(B_TE + tb), par(n - 2, 2), abort_flag, p.wait_limit)))
                     break;
                 if (paged) {
                     const int nblk = (it.kend_max + p.block_size - 1) / p.block_size;
@@ -436,8 +452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             for (int a = 0; a < QT && ok; ++a) {
                 const int qn = 2 * n + a, qs = qn % QSLOTS;
                 if (qn >= QSLOTS &&
-                    !(ok = __all_sync(FULL, mbar_wait(bar(B_QE + qs), par(qn - QSLOTS, QSLOTS), abort_flag,
-                                                      WAIT_LIMIT))))
+                    !(ok = __all_sync(FULL, mbar_wait(bar(B_QE + qs), par(qn - QSLOTS, QSLOTS), abort_flag, p.wait_limit))))
                     break;
                 if (lane == 0) {
                     if (it.rows[a] > 0) {
@@ -450,10 +465,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                     }
                 }
                 __syncwarp();
+                ++qdone;
             }
             if (!ok) break;
             ++n;
         }
+        if (lane == 0) {
+            // the Q tiles in flight land before the CTA's shared memory goes away
+            volatile int32_t dummy = 0;
+            for (int qn = max(0, qdone - QSLOTS); qn < qdone; ++qn)
+                mbar_wait(bar(B_QF + qn % QSLOTS), par(qn, QSLOTS), &dummy, WAIT_LIMIT);
+        }
+        __syncwarp();
     } else if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers (K, V)
         const bool is_k = warp == 0;
@@ -473,7 +496,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             if (w == -2) ok = false;
             if (w < 0) break;
             const int tb = n & 1;
-            if (!(ok = mbar_wait(bar(B_TF + tb), par(n, 2), abort_flag, WAIT_LIMIT))) break;
+            if (!(ok = __all_sync(FULL, mbar_wait(bar(B_TF + tb), par(n, 2), abort_flag, p.wait_limit)))) break;
             const int nblk = paged ? (it.kend_max + p.block_size - 1) / p.block_size : 0;
             src.table = (paged && nblk <= TABLE_SMEM)
                             ? reinterpret_cast<const int32_t *>(smem + OFF_TABLE) + tb * TABLE_SMEM
@@ -481,7 +504,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             src.row0 = it.k0;
             for (int j = 0; j < it.nmax; ++j, ++t) {
                 const int st = t % nst;
-                if (t >= nst && !(ok = mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, WAIT_LIMIT)))
+                if (t >= nst &&
+                    !(ok = __all_sync(FULL, mbar_wait(bar(empty0 + st), par(t - nst, nst), abort_flag, p.wait_limit))))
                     break;
                 load_tile(src, it.g * D, ((SPLIT ? it.jb : 0) + j) * BN, it.kend_max, base + st * TILE_BYTES,
                           bar(full0 + st), lane, p.num_blocks);
@@ -489,12 +513,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             if (!ok) break;
             if (lane == 0) mbar_arrive(bar(B_TE + tb));  // this producer no longer reads the block ids
         }
-        if (*abort_flag && lane == 0) {
-            // let copies already in flight land before the CTA's shared memory goes away
+        if (lane == 0) {
+            // copies still in flight land before the CTA's shared memory goes away
+            // (after a timeout anywhere in the CTA; otherwise these phases are
+            // complete already)
             volatile int32_t dummy = 0;
             for (int u = max(0, t - nst); u < t; ++u)
                 mbar_wait(bar(full0 + u % nst), par(u, nst), &dummy, WAIT_LIMIT);
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Issue blocks while the tensor pipe is busy, so the issue order below is
@@ -517,9 +544,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             if (elect_one()) mma_commit(bar(b));
             __syncwarp();
         };
+        // (a test's stall: this wait runs out after the pipeline limit and the
+        // whole CTA stops as after any timeout)
+        if (p.test_stall) ok = __all_sync(FULL, mbar_wait(bar(B_STALL), 0, abort_flag, p.wait_limit));
         for (int n = 0; ok; ++n) {
             const int slot = n % RING;
-            if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, WAIT_LIMIT))) break;
+            if (!__all_sync(FULL, mbar_wait(bar(B_IRF + slot), par(n, RING), abort_flag, p.wait_limit))) break;
             const int w = ring[slot].w;
             if (w < 0) break;
             const Item it = ring[slot].it;
@@ -528,7 +558,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 0, 1);   // P from TMEM, V MN-major
             auto wait = [&](int b, uint32_t parity) {
-                ok = ok && __all_sync(FULL, mbar_wait(bar(b), parity, abort_flag, WAIT_LIMIT));
+                ok = ok && __all_sync(FULL, mbar_wait(bar(b), parity, abort_flag, p.wait_limit));
                 return ok;
             };
             auto issue_s = [&](int a, int qs, int kst) {
@@ -547,13 +577,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             // previous item, whose P.V was issued before (tcgen05 runs in order)
             if (wait(B_KF + t % KSTAGES, par(t, KSTAGES))) {
                 tc_fence_after();
+                // every Q buffer's landing is waited for in order, used or not, so
+                // that no parity wait runs ahead of an earlier phase of its barrier
                 for (int a = 0; a < QT; ++a) {
                     const int qn = 2 * n + a, qs = qn % QSLOTS;
+                    if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
                     if (it.nt[a] == 0) {
                         commit(B_QE + qs);
                         continue;
                     }
-                    if (!wait(B_QF + qs, par(qn, QSLOTS))) break;
                     tc_fence_after();
                     issue_s(a, qs, t % KSTAGES);
                     if (it.nt[a] == 1) commit(B_QE + qs);  // the tile's last S
@@ -604,8 +636,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             }
             t += it.nmax;
         }
-        if (*abort_flag) {
-            // wait for the MMAs already issued before TMEM and shared memory are released
+        // every MMA issued is complete before TMEM and shared memory are released
+        {
             volatile int32_t dummy = 0;
             commit(B_DRAIN);
             mbar_wait(bar(B_DRAIN), 0, &dummy, WAIT_LIMIT);
@@ -643,7 +675,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             float m_used = -INFINITY;  // running max in scaled base-2 units
             float l = 0.f;
             for (int j = 0; j < it.nt[a]; ++j, ++c) {
-                ok = __all_sync(FULL, mbar_wait(bar(B_SF + a), uint32_t(c) & 1u, abort_flag, WAIT_LIMIT));
+                ok = __all_sync(FULL, mbar_wait(bar(B_SF + a), uint32_t(c) & 1u, abort_flag, p.wait_limit));
                 if (!ok) break;
                 tc_fence_after();
                 const int j0 = (jb + j) * BN;
@@ -677,7 +709,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                 // (before the first half of P is released: P.V of keys 0-63 may read them)
                 if (zeroer && j == it.nmax - 1) {
                     const int tv = tbase + j, sv = tv % VSTAGES;
-                    ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), par(tv, VSTAGES), abort_flag, WAIT_LIMIT));
+                    ok = __all_sync(FULL, mbar_wait(bar(B_VF + sv), par(tv, VSTAGES), abort_flag, p.wait_limit));
                     if (!ok) break;
                     if (j0 + r >= it.kend_max) {
                         uint4 *row0 = reinterpret_cast<uint4 *>(smem + OFF_V + sv * TILE_BYTES + r * 128);
@@ -727,7 +759,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             // epilogue: the item's O of this query tile is complete once its barrier
             // fires; the next item's first P.V (which overwrites O) waits for this
             // warpgroup's next P, written after these reads
-            ok = __all_sync(FULL, mbar_wait(bar(B_OF + a), uint32_t(no) & 1u, abort_flag, WAIT_LIMIT));
+            ok = __all_sync(FULL, mbar_wait(bar(B_OF + a), uint32_t(no) & 1u, abort_flag, p.wait_limit));
             ++no;
             if (!ok) break;
             tc_fence_after();
@@ -780,16 +812,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (*abort_flag) pa::report(p.status, PA_ERR_TIMEOUT);
-        // the last CTA to finish leaves the call's counters at zero for the next call
-        unsigned int *ctr = g_prefill_sched[p.sched_slot];
-        __threadfence();
-        if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
-            atomicExch(ctr, 0u);
-            atomicExch(ctr + 1, 0u);
-        }
-    }
+    if (threadIdx.x == 0 && *abort_flag) pa::report(p.status, PA_ERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -878,11 +901,13 @@ bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int heads, 
 
 int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
 
+
 // How many key ranges each item is split into: 1 when the call has enough
-// items to fill the GPU twice over, otherwise enough splits to do so, each of
-// at least SPLIT_MIN_TILES K/V tiles (a unit's fill and drain cost several
-// tiles' worth of time, so shorter shares do not pay).
-constexpr int SPLIT_MIN_TILES = 6;
+// items to fill the GPU twice over; otherwise the count that minimises
+// rounds x (tiles per unit + a unit's fixed cost, about two tiles' worth of
+// time for its fill and drain), each unit at least SPLIT_MIN_TILES K/V tiles.
+constexpr int SPLIT_MIN_TILES = 4;
+constexpr int UNIT_COST_TILES = 2;
 
 struct PrefillPlan {
     int n_mtiles, n_steps, units, pair_heads, kv_splits;
@@ -902,9 +927,16 @@ PrefillPlan make_prefill_plan(int num_seqs, int max_seqlen_q, int max_seqlen_k, 
     const int64_t want = 2LL * sms;
     const int kv_tiles = (max_seqlen_k + BN - 1) / BN;
     if (pl.items > 0 && pl.items < want && kv_tiles >= 2 * SPLIT_MIN_TILES) {
-        const int64_t by_count = (want + pl.items - 1) / pl.items;
-        const int64_t by_len = kv_tiles / SPLIT_MIN_TILES;
-        pl.kv_splits = int(std::min<int64_t>(std::min<int64_t>(by_count, by_len), 64));
+        const int most = std::min(64, kv_tiles / SPLIT_MIN_TILES);
+        int64_t best = -1;
+        for (int s = 1; s <= most; ++s) {
+            const int64_t rounds = (pl.items * s + sms - 1) / sms;
+            const int64_t cost = rounds * ((kv_tiles + s - 1) / s + UNIT_COST_TILES);
+            if (best < 0 || cost < best) {
+                best = cost;
+                pl.kv_splits = s;
+            }
+        }
     }
     return pl;
 }
@@ -987,8 +1019,9 @@ extern "C" pa_status pa_prefill_paged(const void *q, int64_t q_stride_tok, int64
     p.out = static_cast<uint16_t *>(out);
     p.out_v8 = pa::aligned(out, 32) ? 1 : 0;
     p.status = dev_status;
-    static std::atomic<unsigned> next_slot{0};
-    p.sched_slot = next_slot.fetch_add(1u, std::memory_order_relaxed) % SCHED_SLOTS;
+    // (the waits that drain copies and MMAs after a timeout keep WAIT_LIMIT)
+    p.wait_limit = pa::pipeline_wait_limit(WAIT_LIMIT);
+    p.test_stall = pa::pipeline_test_stall() ? 1 : 0;
     if (!make_rows_map(&p.qmap, q, num_tokens, num_heads, q_stride_tok, BM)) return PA_ERR_CUDA;
     if (block_table != nullptr) {
         const int64_t rows = num_blocks * block_size, row = int64_t(num_kv_heads) * D;

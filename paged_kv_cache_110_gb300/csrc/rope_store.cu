@@ -48,6 +48,8 @@ struct RopeParams {
     int64_t num_slots;
     const int32_t *slots;
     int32_t *status;
+    long long wait_limit;  // SM cycles a pipeline wait may take before the call gives up
+    int test_stall;        // test hook: the compute warps first wait on a barrier nothing arrives on
 };
 
 // Norm (when w != null) and rotate the lane's 4 rotation pairs: lo holds
@@ -125,11 +127,13 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + STAGES * sbytes + 2 * STAGES * 8);
     auto full = [&](int s) { return bars + 8u * uint32_t(s); };
     auto empty = [&](int s) { return bars + 8u * uint32_t(STAGES + s); };
+    const uint32_t stall = bars + 8u * uint32_t(2 * STAGES) + 8u;  // after the abort flag; never arrived on
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), COMPUTE_WARPS);
         }
+        mbar_init(stall, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
                 const int s = k % STAGES;
                 if (k >= STAGES) {
                     ok = __all_sync(FULL, mbar_wait(empty(s), uint32_t((k - STAGES) / STAGES) & 1u, abort_flag,
-                                                    RS_WAIT_LIMIT));
+                                                    p.wait_limit));
                     if (!ok) break;
                 }
                 if (lane == 0) {
@@ -195,10 +199,13 @@ __global__ void __launch_bounds__(RS_THREADS) norm_rope_store_kernel(const RopeP
             wk_hi = *reinterpret_cast<const uint2 *>(p.k_weight + HALF + sub * 4);
         }
         const int iters = (rows + 2 * COMPUTE_WARPS - 1) / (2 * COMPUTE_WARPS);
+        // (a test's stall: this wait runs out after the pipeline limit and the
+        // CTA stops as after any timeout)
+        const bool stalled = p.test_stall && !__all_sync(FULL, mbar_wait(stall, 0, abort_flag, p.wait_limit));
         int k = 0;
-        for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++k) {
+        for (int64_t t = blockIdx.x; !stalled && t < T; t += gridDim.x, ++k) {
             const int s = k % STAGES;
-            if (!__all_sync(FULL, mbar_wait(full(s), uint32_t(k / STAGES) & 1u, abort_flag, RS_WAIT_LIMIT))) break;
+            if (!__all_sync(FULL, mbar_wait(full(s), uint32_t(k / STAGES) & 1u, abort_flag, p.wait_limit))) break;
             const uint8_t *stage = sm + s * sbytes;
             const StageInfo info = *reinterpret_cast<const StageInfo *>(stage + row_bytes + 2 * HALF * 4);
             if (!info.ok) {
@@ -346,6 +353,9 @@ extern "C" pa_status pa_norm_rope_store_kvcache(const void *qkv, int64_t qkv_str
     p.num_slots = num_blocks * block_size;
     p.slots = slot_mapping;
     p.status = dev_status;
+    // (the wait that drains the copies in flight after a timeout keeps RS_WAIT_LIMIT)
+    p.wait_limit = pa::pipeline_wait_limit(RS_WAIT_LIMIT);
+    p.test_stall = pa::pipeline_test_stall() ? 1 : 0;
     // a CTA per token at a time, six CTAs per SM (what shared memory allows at
     // 16 query and 8 KV heads)
     const int rows = num_heads + 2 * num_kv_heads;
