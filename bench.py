@@ -54,11 +54,17 @@ LAYERS = 28
 HQ, HKV, D = wl.HQ, wl.HKV, wl.HEAD_DIM
 ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 
-# DRAM traffic per decode call from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum of the split + merge kernels, decode-batch workload),
-# valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha256": "35b05e8752c91a03b40295e883e21e0b92e6a781586d4fb54e15d012c7c85fec",
-               "bytes_per_call": 587_302_912 + 7_577_344, "kernel": "decode_split_kernel<2, 0>"}
+# DRAM traffic per call from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum; one-pass metrics, clock control off), valid only
+# while the kernel's source file is unchanged:
+#   decode: the split kernel (mean of two launches) + the merge kernel of one
+#     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
+#   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
+NCU_TRAFFIC = {"source_sha256": "17370d6dcd6c0db25e14f0d4c9627d2f277140d882d0f08178dc5a979d8a93dd",
+               "bytes_per_call": 587_134_592 + 6_039_808 + 10_265_088,
+               "kernel": "decode_split_kernel<2, 0> + decode_merge_kernel"}
+NCU_TRAFFIC_PREFILL = {"source_sha256": "ac044416787c9a2a013e213e087d3a13b8255f708baac09df1bfa71a01fc76cb",
+                       "bytes_per_call": 173_679_360 + 35_962_880, "kernel": "prefill_tc_kernel<0>"}
 
 
 def _file_sha(path):
@@ -929,8 +935,11 @@ def main():
     eager_t, eager_bytes = reduce_max_sum(world, elapsed, float(step.step_bytes * args.steps))
     eager_value = eager_bytes / eager_t / 1e9
     unfused_t, unfused_bytes = reduce_max_sum(world, unfused_el, float(step.step_bytes * args.steps))
-    decode_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
+    # the fused call's time inside the graph the headline replays: the step is
+    # exactly `layers` such calls, so the per-call time is the step time / layers
+    decode_s = t_max / args.steps / step.layers
     achieved = step.call_bytes / decode_s / 1e9
+    eager_call_s = sum(s.elapsed_time(e) for s, e in events) / 1e3 / len(events)
 
     e2e = E2EStep(step)
     for _ in range(2):
@@ -976,7 +985,9 @@ def main():
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
                      "traffic": traffic, "traffic_kernel": NCU_TRAFFIC["kernel"],
                      "algorithmic_bytes_per_call": step.call_bytes,
-                     "us_per_call": decode_s * 1e6},
+                     "us_per_call": decode_s * 1e6,
+                     "timing": "per call inside the replayed graph: step time / layers (each layer is one call)",
+                     "eager_us_per_call": eager_call_s * 1e6},
         "clocks": clocks.summary(h0, h1 + 0.25),
     }
     if rank == 0 and not args.no_extras:
@@ -988,7 +999,20 @@ def main():
         pre = time_prefill(device, max(args.steps, 5), 3, flush)
         for v in pre.values():
             v["frac_of_bf16_peak"] = v["tflops"] / peaks["bf16_tflops"]
+            v["tokens_per_s"] = v["query_tokens"] / (v["ms"] / 1e3)
         line["prefill"] = pre
+        vp = pre["varlen_16k"]
+        line["roofline_prefill"] = {
+            "bound": "tensor", "kernel": "prefill_tc_kernel (varlen prefill, 16,384-token budget)",
+            "achieved": vp["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": vp["tflops"] / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 dense (burst)",
+            "algorithmic_flops_per_call": vp["gflop"] * 1e9, "us_per_call": vp["ms"] * 1e3,
+            "counted": "4 * 128 * 16 FLOP per visible (query, key) pair; masked pairs and padding not counted",
+            "traffic": NCU_TRAFFIC_PREFILL["bytes_per_call"] if NCU_TRAFFIC_PREFILL["source_sha256"] == _file_sha(
+                os.path.join(ROOT, "paged_kv_cache_110_gb300", "csrc", "prefill_paged.cu")) else None,
+            "traffic_unit": "bytes per call (DRAM read + write, ncu)"}
+        torch.cuda.empty_cache()
+        line["block_sizes"] = time_block_size_sweep(device, 5, 2, flush)
         torch.cuda.empty_cache()
         ld = time_long_decode(device, max(args.steps, 5), 3, flush)
         ld["frac"] = ld["gbs"] / peaks["hbm_gbs"]
