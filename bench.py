@@ -710,6 +710,60 @@ def time_mixed(device, steps, warmup, flush):
     return res
 
 
+def time_decode_layer_step(device, steps, warmup, layers=LAYERS):
+    """The decode step of the attention layers with the head norm and RoPE of
+    the new tokens included (the decode-batch workload, 28 layers, graph-
+    captured): per layer either pa_norm_rope_store_decode_paged (one call), or
+    pa_norm_rope_store_kvcache followed by pa_decode_paged (two calls)."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    step = DecodeStep(device, layers=layers)
+    cs = pa.pa_rope_cos_sin_table(wl.ROPE_BASE, D, 4096, device=device)
+    qw, kw = wl.norm_weights(21, device=device)
+    pos = torch.as_tensor((step.ctx - 1).astype(np.int32), device=device)
+    q_out = [torch.empty((step.B, HQ, D), dtype=torch.bfloat16, device=device) for _ in range(layers)]
+
+    def fused():
+        for l in range(layers):
+            pa.pa_norm_rope_store_decode_paged(step.tokens[l].qkv, HQ, HKV, cs, qw, kw, wl.RMS_EPS, step.k_cache[l],
+                                               step.v_cache[l], step.tables, step.ctx_t, step.max_ctx, wl.SCALE,
+                                               step.out[l], step.ws)
+
+    def two():
+        for l in range(layers):
+            pa.pa_norm_rope_store_kvcache(step.tokens[l].qkv, HQ, HKV, pos, cs, qw, kw, wl.RMS_EPS, q_out[l],
+                                          step.k_cache[l], step.v_cache[l], step.slots)
+            pa.pa_decode_paged(q_out[l], step.k_cache[l], step.v_cache[l], step.tables, step.ctx_t, step.max_ctx,
+                               wl.SCALE, step.out[l], step.ws)
+
+    res = {}
+    for name, fn in (("one_call", fused), ("two_calls", two)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(steps):
+            g.replay()
+        e0.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(e0) / steps
+        res[name] = {"ms_per_step": ms, "us_per_layer": ms / layers * 1e3}
+        del g
+    res["workload"] = ("decode batch x 28 layers (256 seqs, context U[100,1024], block_size 256): head RMSNorm + "
+                       "RoPE of q and k, KV write and paged decode per layer, graph-captured")
+    return res
+
+
 def time_step_metadata(device, steps, warmup):
     """Device-built step metadata: the varlen-prefill batch (counts and tables
     of ~20 sequences, 16K tokens expanded) and a 512-sequence decode batch;
@@ -842,7 +896,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
     ap.add_argument("--leg", default="all",
                     choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8",
-                             "block_sizes"],
+                             "block_sizes", "decode_layer"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all",
                     choices=["all", "varlen_16k", "prefix_2048_chunked", "chunk_512_over_8k"])
@@ -870,6 +924,8 @@ def main():
             res = time_block_size_sweep(device, max(args.steps, 1), args.warmup, flush)
         elif args.leg == "mixed":
             res = time_mixed(device, max(args.steps, 1), args.warmup, flush)
+        elif args.leg == "decode_layer":
+            res = time_decode_layer_step(device, max(args.steps, 1), args.warmup)
         elif args.leg == "metadata":
             res = time_step_metadata(device, max(args.steps, 1), args.warmup)
         elif args.leg == "rope_store":
@@ -1023,6 +1079,8 @@ def main():
             v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         line["norm_rope_store"] = rs
         line["step_metadata"] = time_step_metadata(device, max(args.steps, 5), 3)
+        torch.cuda.empty_cache()
+        line["decode_layer_step"] = time_decode_layer_step(device, 50, 3)
         torch.cuda.empty_cache()
         line["mixed_step"] = time_mixed(device, max(args.steps, 5), 3, flush)
         torch.cuda.empty_cache()

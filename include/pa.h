@@ -319,6 +319,41 @@ pa_status pa_store_decode_paged(const void *q, int64_t q_stride_seq, const void 
                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * The attention decode step of one layer from the fused QKV projection's
+ * output, in one launch (plus the split merge): the per-head RMSNorm and RoPE
+ * of the new token ("nano-vllm 技术分析" §4.3-4.4; "大模型推理入门与 nano-vLLM
+ * 源码详解" §19.3, §19.7, §12.2), its KV write and the paged decode.  For every
+ * sequence b with context_lens[b] > 0, at position p = context_lens[b] - 1:
+ *   - each query head and key head of qkv[b] is normalised and rotated as in
+ *     pa_norm_rope_store_kvcache (norm skipped without its weight; cos / sin
+ *     from row p of cos_sin);
+ *   - the rotated key heads and the unchanged value heads go to the pool row
+ *     of position p (through block_table), as pa_store_decode_paged writes;
+ *   - the rotated query attends to keys 0 .. p as in pa_decode_paged.
+ * The result equals pa_norm_rope_store_kvcache (positions p, slots the rows
+ * of p) followed by pa_decode_paged over its q_out, up to the bf16 rounding
+ * of the normalised values (the sum of squares is added in another order).
+ *
+ *   qkv           [num_seqs, (num_heads + 2 num_kv_heads) * head_dim] bf16:
+ *                 query heads, key heads, value heads; sequence stride
+ *                 qkv_stride_seq elements (a multiple of 8); 16-byte aligned.
+ *   cos_sin, max_positions, q_norm_weight, k_norm_weight, eps   as for
+ *                 pa_norm_rope_store_kvcache; a position at or past
+ *                 max_positions sets PA_ERR_BOUNDS and that sequence's output
+ *                 is zero and its row is not written.
+ *   Every other argument, the workspace and the errors as
+ *   pa_store_decode_paged.
+ */
+pa_status pa_norm_rope_store_decode_paged(const void *qkv, int64_t qkv_stride_seq, const float *cos_sin,
+                                          int64_t max_positions, const void *q_norm_weight,
+                                          const void *k_norm_weight, float eps, void *k_cache, void *v_cache,
+                                          int64_t num_blocks, int block_size, const int32_t *block_table,
+                                          int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                          int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                                          float scale, void *out, void *workspace, size_t workspace_bytes,
+                                          int32_t *dev_status, void *stream);
+
+/*
  * fp8 KV cache ("大模型推理入门与 nano-vLLM 源码详解" §17.3 names the KV
  * precision as the lever for longer contexts; "VLLM on Fain的Blog" counts FP8
  * at one byte per element.  The pages fix no format; this library's is the

@@ -20,7 +20,7 @@ __all__ = [
     "pa_store_kvcache", "pa_store_kvcache_fp8", "pa_norm_rope_store_kvcache", "pa_rope_cos_sin_table",
     "pa_prepare_prefill", "pa_prepare_decode", "pa_prefill_workspace_bytes", "pa_prefill_paged",
     "pa_decode_workspace_bytes", "pa_decode_paged", "pa_store_decode_paged", "pa_decode_paged_fp8",
-    "pa_decode_paged_noalloc", "pa_test_stall_pipelines",
+    "pa_decode_paged_noalloc", "pa_test_stall_pipelines", "pa_norm_rope_store_decode_paged",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_TIMEOUT = range(6)
@@ -73,6 +73,9 @@ def _load() -> ctypes.CDLL:
     L.pa_store_decode_paged.restype = i32
     L.pa_store_decode_paged.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                         f32, vp, vp, sz, vp, vp]
+    L.pa_norm_rope_store_decode_paged.restype = i32
+    L.pa_norm_rope_store_decode_paged.argtypes = [vp, i64, vp, i64, vp, vp, f32, vp, vp, i64, i32, vp, i32, vp, i32,
+                                                  i32, i32, i32, i32, f32, vp, vp, sz, vp, vp]
     L.pa_test_stall_pipelines.restype = None
     L.pa_test_stall_pipelines.argtypes = [ctypes.c_longlong]
     L.pa_decode_paged_noalloc.restype = i32
@@ -376,6 +379,40 @@ def pa_store_decode_paged(q, k_new, v_new, k_cache, v_cache, block_table, contex
                                      int(max_context_len), hq, hkv, d, float(scale), _ptr(out), _ptr(workspace),
                                      ws_bytes, _ptr(dev_status), _stream(stream)),
            "pa_store_decode_paged")
+
+
+def pa_norm_rope_store_decode_paged(qkv, num_heads, num_kv_heads, cos_sin, q_norm_weight, k_norm_weight, eps, k_cache,
+                                    v_cache, block_table, context_lens, max_context_len, scale, out, workspace,
+                                    dev_status=None, stream=None):
+    """One layer's decode step from the fused QKV output: qkv [B, (Hq + 2 Hkv) * 128] bf16 (sequence stride free);
+    head norm + RoPE of the new token at position context_lens[b] - 1, its K/V to that position's pool row, then
+    decode as pa_decode_paged.  out [B, Hq, 128] packed; workspace as for pa_decode_paged."""
+    if qkv.dtype != torch.bfloat16 or qkv.dim() != 2 or not qkv.is_cuda or qkv.stride(1) != 1:
+        raise TypeError("qkv: expected a CUDA bf16 [B, (Hq + 2 Hkv) * D] tensor with packed columns")
+    nb, bs, hkv, d = _cache(k_cache, "k_cache")
+    _cache(v_cache, "v_cache")
+    if hkv != num_kv_heads or qkv.shape[1] != (num_heads + 2 * num_kv_heads) * d:
+        raise ValueError("qkv columns do not match num_heads / num_kv_heads and the cache")
+    if cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or not cos_sin.is_contiguous() or cos_sin.shape[1] != d:
+        raise TypeError("cos_sin: expected a contiguous CUDA fp32 [max_positions, head_dim] tensor")
+    for w, name in ((q_norm_weight, "q_norm_weight"), (k_norm_weight, "k_norm_weight")):
+        if w is not None and (w.dtype != torch.bfloat16 or w.numel() != d or not w.is_contiguous()):
+            raise TypeError(f"{name}: expected a contiguous bf16 [head_dim] tensor or None")
+    _i32(block_table, "block_table")
+    _i32(context_lens, "context_lens")
+    b = qkv.shape[0]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.shape != (b, num_heads, d):
+        raise ValueError("out must be a contiguous bf16 [B, Hq, D] tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != b or context_lens.numel() != b:
+        raise ValueError("block_table / context_lens do not match qkv")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_norm_rope_store_decode_paged(_ptr(qkv), qkv.stride(0), _ptr(cos_sin), cos_sin.shape[0],
+                                               _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps), _ptr(k_cache),
+                                               _ptr(v_cache), nb, bs, _ptr(block_table), block_table.shape[1],
+                                               _ptr(context_lens), b, int(max_context_len), num_heads, hkv, d,
+                                               float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                               _stream(stream)),
+           "pa_norm_rope_store_decode_paged")
 
 
 def pa_decode_paged_noalloc(q, k_cache, v_cache, block_table, context_lens, max_context_len, scale, out,

@@ -64,6 +64,11 @@ struct DecodeParams {
     const uint16_t *k_new;  // fused KV write: the step's new K / V rows [num_seqs][kv_heads][D], or null
     const uint16_t *v_new;
     int64_t kv_new_stride;  // elements between sequences' rows of k_new / v_new
+    // head norm + RoPE of the step's new token (q, and k_new before it is stored), or cos_sin == null
+    const float *cos_sin;   // [max_positions][D]: cos of the 64 pairs, then sin
+    int64_t max_positions;
+    const uint16_t *q_weight, *k_weight;  // [D] bf16, or null: no norm
+    float eps;
     float *ws_o;      // [num_seqs][max_splits][num_heads][D]
     float2 *ws_ml;    // [num_seqs][max_splits][num_heads] (max, sum), base-2
     int split_len;
@@ -154,6 +159,77 @@ struct KvRow<true> {
     static __device__ __forceinline__ Raw zero() { return make_uint2(0, 0); }
 };
 
+// RMSNorm (when `norm`: v = bf16(bf16(v / rms) * w), w = 1 without a weight)
+// and RoPE of one head row of the step's new token, held as 8 features per
+// lane by the 16 lanes of a half-warp (lane c: features 8c .. 8c+7).  Feature
+// i pairs with feature i + 64, which sits in lane c ^ 8: (a, b) ->
+// (a cos - b sin, a sin + b cos) in fp32, rounded to bf16 ("nano-vllm 技术分析"
+// §4.3-4.4; "大模型推理入门与 nano-vLLM 源码详解" §19.3, §19.7).  The steps
+// and their roundings are those of the fused norm + RoPE + KV write.  Every
+// lane of the warp calls this with the same `norm` (the sum of squares is
+// reduced over the half-warp and the partners exchanged by shuffles).
+__device__ __forceinline__ void norm_rope_row8(float (&x)[8], int c, bool norm, const float (&wv)[8], float eps,
+                                               const float (&cv)[8], const float (&sv)[8])
+{
+    if (norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+        const float r = 1.0f / sqrtf(ss * (1.0f / D) + eps);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const uint32_t t = pa::pack_bf16x2(x[e] * r, x[e + 1] * r);
+            const uint32_t u = pa::pack_bf16x2(pa::bf16_lo(t) * wv[e], pa::bf16_hi(t) * wv[e + 1]);
+            x[e] = pa::bf16_lo(u);
+            x[e + 1] = pa::bf16_hi(u);
+        }
+    }
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(FULL, x[e], 8);
+    float out[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        out[e] = (c < 8) ? fmaf(x[e], cv[e], -y[e] * sv[e])   // a' = a cos - b sin (x = a, y = b)
+                         : fmaf(y[e], sv[e], x[e] * cv[e]);   // b' = a sin + b cos (y = a, x = b)
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const uint32_t u = pa::pack_bf16x2(out[e], out[e + 1]);
+        x[e] = pa::bf16_lo(u);
+        x[e + 1] = pa::bf16_hi(u);
+    }
+}
+
+// The norm weight (8 features of lane c, 1 without a weight) and the cos / sin
+// of lane c's 8 pairs at one position (row cs of the table).
+struct RopeLane {
+    float w[8], c[8], s[8];
+};
+__device__ __forceinline__ RopeLane rope_lane(const uint16_t *w, const float *cs, int c)
+{
+    RopeLane r;
+    if (w != nullptr) {
+        unpack8(*reinterpret_cast<const uint4 *>(w + 8 * c), r.w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r.w[e] = 1.f;
+    }
+    const float4 *cp = reinterpret_cast<const float4 *>(cs + 8 * (c & 7));
+    const float4 *sp = reinterpret_cast<const float4 *>(cs + D / 2 + 8 * (c & 7));
+    const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
+    r.c[0] = c0.x; r.c[1] = c0.y; r.c[2] = c0.z; r.c[3] = c0.w; r.c[4] = c1.x; r.c[5] = c1.y; r.c[6] = c1.z; r.c[7] = c1.w;
+    r.s[0] = s0.x; r.s[1] = s0.y; r.s[2] = s0.z; r.s[3] = s0.w; r.s[4] = s1.x; r.s[5] = s1.y; r.s[6] = s1.z; r.s[7] = s1.w;
+    return r;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+{
+    return make_uint4(pa::pack_bf16x2(f[0], f[1]), pa::pack_bf16x2(f[2], f[3]), pa::pack_bf16x2(f[4], f[5]),
+                      pa::pack_bf16x2(f[6], f[7]));
+}
+
 // One transposing butterfly step over the 16 lanes of a half-warp: lanes
 // whose bit M is set keep the upper half of x, the others the lower half,
 // and each adds its partner's copy of the half it keeps.  With N == 1 it is
@@ -188,7 +264,7 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-template <int G, bool FP8>
+template <int G, bool FP8, bool ROPE>
 __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
 {
     using KV = KvRow<FP8>;
@@ -202,7 +278,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     pa::grid_dependency_wait();
 
     int ctx = p.context_lens[b];
-    if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) {
+    if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size ||
+        (ROPE && int64_t(ctx) > p.max_positions)) {
         if (s == 0 && threadIdx.x == 0) pa::report(p.status, PA_ERR_BOUNDS);
         ctx = 0;
     }
@@ -235,12 +312,22 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
             new_tok = ctx - 1;
             if (sub == 0) {
                 const int32_t phys = table[new_tok / p.block_size];
+                const uint16_t *src = (half ? p.v_new : p.k_new) + int64_t(b) * p.kv_new_stride + g * D + 8 * c;
+                uint4 u = *reinterpret_cast<const uint4 *>(src);
+                if constexpr (ROPE) {
+                    // K (lanes 0-15) normalised and rotated before it is stored; the V
+                    // lanes take part in the shuffles and store their row unchanged
+                    const RopeLane rl = rope_lane(p.k_weight, p.cos_sin + int64_t(new_tok) * D, c);
+                    float x[8];
+                    unpack8(u, x);
+                    norm_rope_row8(x, c, p.k_weight != nullptr, rl.w, p.eps, rl.c, rl.s);
+                    if (!half) u = pack8(x);
+                }
                 if (phys >= 0 && int64_t(phys) < p.num_blocks) {
                     const int64_t row = int64_t(phys) * p.block_size + new_tok % p.block_size;
-                    const uint16_t *src = (half ? p.v_new : p.k_new) + int64_t(b) * p.kv_new_stride + g * D + 8 * c;
                     uint16_t *dst = static_cast<uint16_t *>(const_cast<void *>(half ? p.v_cache : p.k_cache)) +
                                     row * row_elems + g * D + 8 * c;
-                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                    *reinterpret_cast<uint4 *>(dst) = u;
                 }
                 // an invalid block id is reported by the loop below, which skips that chunk
             }
@@ -248,13 +335,37 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
     }
 
+    if (g == 0 && lane == 0) {
+        // bring this warp group's first chunk (all KV heads, one contiguous run) into L2
+        const int cf = t0 + sub * CHUNK;
+        if (cf < t1) {
+            const int32_t pf = table[cf / p.block_size];
+            if (pf >= 0 && int64_t(pf) < p.num_blocks) {
+                const int64_t r = (int64_t(pf) * p.block_size + cf % p.block_size) * row_elems;
+                const uint32_t bytes = uint32_t(min(CHUNK, t1 - cf) * row_elems * sizeof(typename KV::Elem));
+                const uint32_t b16 = (bytes + 15u) & ~15u;
+                pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.k_cache) + r, b16);
+                pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.v_cache) + r, b16);
+            }
+        }
+    }
     float qf[G][8];
+    {
+        uint4 qr[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + h) * D + 8 * c);
-        unpack8(u, qf[h]);
+        for (int h = 0; h < G; ++h)
+            qr[h] = *reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + h) * D + 8 * c);
+        RopeLane rl;
+        // every split rotates the query itself (a few hundred flops); its weight
+        // and cos / sin are loaded together with the row: one round trip
+        if constexpr (ROPE) rl = rope_lane(p.q_weight, p.cos_sin + int64_t(ctx - 1) * D, c);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
+        for (int h = 0; h < G; ++h) {
+            unpack8(qr[h], qf[h]);
+            if constexpr (ROPE) norm_rope_row8(qf[h], c, p.q_weight != nullptr, rl.w, p.eps, rl.c, rl.s);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
+        }
     }
     float o[G][8];
     float m[G], l[G];
@@ -474,33 +585,27 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 
 // Merge the split partials of every sequence that has more than one split
 // ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
-// L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.
+// L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.  A thread per
+// (head, 8 columns); the statistics and partials of eight splits are loaded
+// together, so that up to eight splits cost one round trip to L2; more are
+// combined eight at a time, the running (M, L, out) rescaled as M grows.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 {
     pa::grid_dependency_wait();  // the split kernel's partials
     pa::grid_dependents_launch();
     const int b = blockIdx.x;
     int ctx = p.context_lens[b];
-    if (ctx <= 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) return;
+    if (ctx <= 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size ||
+        (p.cos_sin != nullptr && int64_t(ctx) > p.max_positions))
+        return;
     const int nsplit = (ctx + p.split_len - 1) / p.split_len;
     if (nsplit <= 1) return;
     for (int item = threadIdx.x; item < p.num_heads * (D / 8); item += blockDim.x) {
         const int h = item / (D / 8), c = item % (D / 8);
         const int64_t base = int64_t(b) * p.max_splits * p.num_heads + h;
-        // MS splits' loads are issued together, so a pass costs one round trip
-        // per MS splits, not one per split
         constexpr int MS = 8;
-        float mm = -INFINITY;
-        for (int t0 = 0; t0 < nsplit; t0 += MS) {
-            float mv[MS];
-#pragma unroll
-            for (int u = 0; u < MS; ++u)
-                mv[u] = t0 + u < nsplit ? p.ws_ml[base + int64_t(t0 + u) * p.num_heads].x : -INFINITY;
-#pragma unroll
-            for (int u = 0; u < MS; ++u) mm = fmaxf(mm, mv[u]);
-        }
+        float mm = -INFINITY, ll = 0.f;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float ll = 0.f;
         for (int t0 = 0; t0 < nsplit; t0 += MS) {
             float2 ml[MS];
             float4 x0[MS], x1[MS];
@@ -517,6 +622,14 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
                     x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            float gm = mm;
+#pragma unroll
+            for (int u = 0; u < MS; ++u) gm = fmaxf(gm, ml[u].x);
+            const float a = (mm == -INFINITY) ? 0.f : exp2f(mm - gm);
+            ll *= a;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= a;
+            mm = gm;
 #pragma unroll
             for (int u = 0; u < MS; ++u) {
                 const float w = (ml[u].x == -INFINITY) ? 0.f : exp2f(ml[u].x - mm);
@@ -539,7 +652,10 @@ template <int G, bool FP8>
 void launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
-    pa::launch_pdl(decode_split_kernel<G, FP8>, grid, dim3(NW * 32), 0, stream, p);
+    if (!FP8 && p.cos_sin != nullptr)
+        pa::launch_pdl(decode_split_kernel<G, FP8, !FP8>, grid, dim3(NW * 32), 0, stream, p);
+    else
+        pa::launch_pdl(decode_split_kernel<G, FP8, false>, grid, dim3(NW * 32), 0, stream, p);
 }
 
 pa_status check_args(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
@@ -576,7 +692,9 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int max_context_len,
                       int num_heads, int num_kv_heads, int head_dim, float scale, void *out, void *workspace,
                       size_t workspace_bytes_given, int32_t *dev_status, void *stream, const void *k_new = nullptr,
-                      const void *v_new = nullptr, int64_t kv_new_stride = 0)
+                      const void *v_new = nullptr, int64_t kv_new_stride = 0, const float *cos_sin = nullptr,
+                      int64_t max_positions = 0, const void *q_weight = nullptr, const void *k_weight = nullptr,
+                      float eps = 0.f)
 {
     pa_status st = check_args(q, q_stride_seq, k_cache, v_cache, num_blocks, block_size, block_table,
                               max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
@@ -608,6 +726,11 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.kv_new_stride = kv_new_stride;
+    p.cos_sin = cos_sin;
+    p.max_positions = max_positions;
+    p.q_weight = static_cast<const uint16_t *>(q_weight);
+    p.k_weight = static_cast<const uint16_t *>(k_weight);
+    p.eps = eps;
     const size_t n = size_t(num_seqs) * (plan.max_splits > 0 ? plan.max_splits : 1) * num_heads;
     p.ws_o = static_cast<float *>(workspace);
     p.ws_ml = need > 0 ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
@@ -672,6 +795,39 @@ extern "C" pa_status pa_store_decode_paged(const void *q, int64_t q_stride_seq, 
                        max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
                        head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream, k_new, v_new,
                        kv_new_stride_seq);
+}
+
+// The decode step of one layer from the fused QKV projection's output, in one
+// launch (plus the merge): q and the new k get the head norm and RoPE at
+// position context_lens[b] - 1, the new k and v go to that position's pool row
+// (through the block table), and the decode runs as pa_store_decode_paged's.
+extern "C" pa_status pa_norm_rope_store_decode_paged(const void *qkv, int64_t qkv_stride_seq, const float *cos_sin,
+                                                     int64_t max_positions, const void *q_norm_weight,
+                                                     const void *k_norm_weight, float eps, void *k_cache,
+                                                     void *v_cache, int64_t num_blocks, int block_size,
+                                                     const int32_t *block_table, int max_blocks_per_seq,
+                                                     const int32_t *context_lens, int num_seqs, int max_context_len,
+                                                     int num_heads, int num_kv_heads, int head_dim, float scale,
+                                                     void *out, void *workspace, size_t workspace_bytes_given,
+                                                     int32_t *dev_status, void *stream)
+{
+    if (num_seqs > 0) {
+        if (qkv == nullptr || cos_sin == nullptr || !pa::aligned(qkv, 16) || !pa::aligned(cos_sin, 16) ||
+            max_positions < 1 || !(eps >= 0.f))
+            return PA_ERR_INVALID_ARG;
+        if (num_heads <= 0 || num_kv_heads <= 0 ||
+            qkv_stride_seq < int64_t(num_heads + 2 * num_kv_heads) * head_dim || qkv_stride_seq % 8 != 0)
+            return PA_ERR_INVALID_ARG;
+        if ((q_norm_weight && !pa::aligned(q_norm_weight, 16)) || (k_norm_weight && !pa::aligned(k_norm_weight, 16)))
+            return PA_ERR_INVALID_ARG;
+    }
+    const uint16_t *base = static_cast<const uint16_t *>(qkv);
+    const int64_t kcol = int64_t(num_heads) * head_dim, vcol = kcol + int64_t(num_kv_heads) * head_dim;
+    return decode_impl(qkv, qkv_stride_seq, k_cache, v_cache, false, 1.f, 1.f, num_blocks, block_size, block_table,
+                       max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                       head_dim, scale, out, workspace, workspace_bytes_given, dev_status, stream,
+                       num_seqs > 0 ? base + kcol : nullptr, num_seqs > 0 ? base + vcol : nullptr, qkv_stride_seq,
+                       cos_sin, max_positions, q_norm_weight, k_norm_weight, eps);
 }
 
 // Decode over fp8 (E4M3) pools written by pa_store_kvcache_fp8: the same
