@@ -60,8 +60,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 #   decode: the split kernel (mean of two launches) + the merge kernel of one
 #     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
 #   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
-NCU_TRAFFIC = {"source_sha256": "17370d6dcd6c0db25e14f0d4c9627d2f277140d882d0f08178dc5a979d8a93dd",
-               "bytes_per_call": 587_134_592 + 6_039_808 + 10_265_088,
+NCU_TRAFFIC = {"source_sha256": "2a8b07e22aa6c13a00003e900eed219af4f58cbd330d16640f142754af467686",
+               "bytes_per_call": 587_273_984 + 6_572_032 + 10_265_600,
                "kernel": "decode_split_kernel<2, 0> + decode_merge_kernel"}
 NCU_TRAFFIC_PREFILL = {"source_sha256": "ac044416787c9a2a013e213e087d3a13b8255f708baac09df1bfa71a01fc76cb",
                        "bytes_per_call": 173_679_360 + 35_962_880, "kernel": "prefill_tc_kernel<0>"}
