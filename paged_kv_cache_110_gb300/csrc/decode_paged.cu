@@ -41,6 +41,7 @@ constexpr int D = pa::kHeadDim;
 constexpr int NW = 8;          // warps per CTA
 constexpr int CHUNK = 16;      // tokens per warp iteration (8 per half-warp)
 constexpr int PREFETCH_CHUNKS = 1;  // how many of a warp's chunks ahead to prefetch into L2
+constexpr int PREFETCH_CHUNKS_FP8 = 1;  // the same for fp8 pools (half the bytes per chunk)
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -118,45 +119,13 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
     f[6] = pa::bf16_lo(u.w); f[7] = pa::bf16_hi(u.w);
 }
 
-// 8 E4M3 codes (little-endian in u) to floats, exactly (through f16).
-__device__ __forceinline__ void unpack8(const uint2 &u, float (&f)[8])
-{
-    const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w[i] >> (16 * j)), __NV_E4M3);
-            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&r));
-            f[4 * i + 2 * j] = v.x;
-            f[4 * i + 2 * j + 1] = v.y;
-        }
-    }
-}
-
-__device__ __forceinline__ uint2 ld_stream8(const void *p)
-{
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
-
-// The pool's element type: bf16 rows (16 bytes per lane load) or E4M3 rows (8).
-template <bool FP8>
+// A bf16 pool row piece: 8 elements (16 bytes) per lane load.
 struct KvRow {
     using Raw = uint4;
     using Elem = uint16_t;
     static __device__ __forceinline__ Raw load(const Elem *p) { return pa::ld_stream16(p); }
     static __device__ __forceinline__ Raw load_l2(const Elem *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
     static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
-};
-template <>
-struct KvRow<true> {
-    using Raw = uint2;
-    using Elem = uint8_t;
-    static __device__ __forceinline__ Raw load(const Elem *p) { return ld_stream8(p); }
-    static __device__ __forceinline__ Raw load_l2(const Elem *p) { return __ldcg(reinterpret_cast<const uint2 *>(p)); }
-    static __device__ __forceinline__ Raw zero() { return make_uint2(0, 0); }
 };
 
 // RMSNorm (when `norm`: v = bf16(bf16(v / rms) * w), w = 1 without a weight)
@@ -264,10 +233,10 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-template <int G, bool FP8, bool ROPE>
+template <int G, bool ROPE>
 __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
 {
-    using KV = KvRow<FP8>;
+    using KV = KvRow;
     constexpr int V = 8 * G;                 // partial dot products per lane per chunk
     constexpr int R = V >= 16 ? V / 16 : 1;  // whole dot products per lane after the butterfly
     const int b = blockIdx.x, s = blockIdx.y;
@@ -307,7 +276,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     // this launch, after the barrier below, and the chunk that holds it is read
     // through L2 (ld.global.cg), not the read-only path the other chunks use.
     int new_tok = -1;  // position written by this launch, or -1
-    if constexpr (!FP8) {
+    {
         if (p.k_new != nullptr && s == nsplit - 1) {  // the same for the whole CTA
             new_tok = ctx - 1;
             if (sub == 0) {
@@ -405,7 +374,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
 
         typename KV::Raw kr[8], vr[8];
-        if (!FP8 && unsigned(new_tok - cb) < unsigned(CHUNK)) {
+        if (unsigned(new_tok - cb) < unsigned(CHUNK)) {
             // the chunk holding the row this launch wrote: coherent loads through L2
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -438,20 +407,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
             unpack8(kr[i], kf);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                if constexpr (FP8) {
-                    // fp8 pools are bound by instruction issue (each element also needs a
-                    // conversion): paired fp32 FMAs, two partial sums, half the FMAs
-                    float a0 = 0.f, a1 = 0.f;
+                float acc = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        pa::sm100::ffma2(a0, a1, qf[h][e], qf[h][e + 1], kf[e], kf[e + 1], a0, a1);
-                    x[i * G + h] = a0 + a1;
-                } else {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-                    x[i * G + h] = acc;
-                }
+                for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+                x[i * G + h] = acc;
             }
         }
         xpose_step<V, 8>(x, c);
@@ -498,14 +457,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
                 const int idx = i * G + h;
                 const int src_c = (G == 1) ? 2 * i : idx / R;
                 const float pv = __shfl_sync(FULL, pr[(G == 1) ? 0 : idx % R], src_c, 16);
-                if constexpr (FP8) {
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        pa::sm100::ffma2(o[h][e], o[h][e + 1], pv, pv, vf[e], vf[e + 1], o[h][e], o[h][e + 1]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pv, vf[e], o[h][e]);
-                }
+                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pv, vf[e], o[h][e]);
             }
         }
     }
@@ -583,6 +536,297 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode over E4M3 pools on the warp-level tensor-core MMA (mma.sync
+// m16n8k16: f16 operands, f32 accumulators).
+//
+// Converting every E4M3 code to f32 for CUDA-core FMAs costs more instruction
+// issue than the byte is worth, so fp8 pools would leave HBM idle that way.
+// Here one conversion instruction turns two codes into an f16 pair (exact:
+// every E4M3 value is an f16 value) and the dot products and the P.V sums run
+// as MMAs; the K scale is folded into the score scale and the V scale into the
+// output, as for the CUDA-core path.  The work split is the bf16 kernel's:
+// CTA = (sequence, split), warp = (KV head, every wph-th 16-token chunk).
+// Lane (gq, tq) = (lane / 4, lane % 4).  Per chunk:
+//   S = Q K^T   A = the group's G query heads (rows 0..G-1 of 16, f16; each
+//               head multiplied by the power of two that puts its largest
+//               magnitude in [2^13, 2^14), undone on the fp32 score), B = the
+//               keys of an 8-token block; two blocks x 8 steps of 16 dims.
+//               Lane (gq, tq) supplies token gq of a block, dims 32 tq ..
+//               32 tq + 31: each step takes the dims in an order of its own,
+//               the query the same, so that a lane reads 32 contiguous bytes.
+//   softmax     the accumulator holds head gq's scores of tokens 2tq, 2tq+1
+//               and 8+2tq, 9+2tq: max and sum over the 4 lanes of head gq.
+//               The running max moves only when a score passes it by more than
+//               2^8 (log2 units), so O is rarely rescaled; O / l uses the same
+//               max, so the result does not depend on when it moved.
+//   O^T += V^T P^T   A = V^T (16 dims x the 16 tokens): lane gq supplies dims
+//               16 gq .. 16 gq + 15 of tokens 2tq, 2tq+1, 2tq+8, 2tq+9, two
+//               tokens' codes interleaved by a byte permute before the
+//               conversion; B = P^T (f16), which is the S accumulator's layout
+//               as it stands; C = O^T, 8 blocks of 16 dims x 8 head columns.
+// Rounding: the products of f16 operands are exact in the f32 accumulators
+// (q is a bf16 value times a power of two, exactly an f16 value in the range
+// the prescale gives); P (below 2^8) is rounded to f16 (relative 2^-11) for
+// the P.V MMA.
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(two_codes & 0xffffu), __NV_E4M3);
+    return uint32_t(r.x) | (uint32_t(r.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// d += A (16 x 16, row) * B (16 x 8, col), f16 in, f32 accumulate
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr float FP8_RESCALE_THRESHOLD = 8.0f;  // log2 units
+
+template <int G>
+__global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const DecodeParams p)
+{
+    const int b = blockIdx.x, s = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    pa::grid_dependency_wait();
+
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) {
+        if (s == 0 && threadIdx.x == 0) pa::report(p.status, PA_ERR_BOUNDS);
+        ctx = 0;
+    }
+    if (ctx == 0) {  // padded row: output zeros, read nothing
+        if (s == 0) {
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.num_heads * D);
+            for (int i = threadIdx.x; i < p.num_heads * D / 8; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    const int nsplit = (ctx + p.split_len - 1) / p.split_len;
+    if (s >= nsplit) return;
+
+    const int g = warp % p.kv_heads;
+    const int sub = warp / p.kv_heads;
+    const int wph = NW / p.kv_heads;
+    const int t0 = s * p.split_len;
+    const int t1 = min(ctx, t0 + p.split_len);
+    const int row_elems = p.kv_heads * D;
+    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+    const uint8_t *kc = static_cast<const uint8_t *>(p.k_cache);
+    const uint8_t *vc = static_cast<const uint8_t *>(p.v_cache);
+
+    auto prefetch_chunk = [&](int cf) {  // a chunk's 16 rows of all KV heads: one contiguous run of one block
+        if (cf >= t1) return;
+        const int32_t pf = table[cf / p.block_size];
+        if (pf < 0 || int64_t(pf) >= p.num_blocks) return;
+        const int64_t r = (int64_t(pf) * p.block_size + cf % p.block_size) * row_elems;
+        const uint32_t bytes = uint32_t(min(CHUNK, t1 - cf) * row_elems);
+        const uint32_t b16 = (bytes + 15u) & ~15u;
+        pa::sm100::prefetch_l2_bulk(kc + r, b16);
+        pa::sm100::prefetch_l2_bulk(vc + r, b16);
+    };
+    if (g == 0 && lane == 0) prefetch_chunk(t0 + sub * CHUNK);
+
+    // the query: head gq of the group (rows gq >= G stay zero), dims 32 tq .. 32 tq + 31
+    uint32_t qa[8][2];
+    float sscale;  // score scale of head gq in log2 units, the prescale undone
+    {
+        float x[32];
+        if (gq < G) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + gq) * D + 32 * tq);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float f[8];
+                unpack8(qp[i], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[8 * i + e] = f[e];
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+        }
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(x[e]));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+        int k = 0;
+        if (mx > 0.f) k = min(126, max(-126, 13 - (int((__float_as_uint(mx) >> 23) & 0xffu) - 127)));
+        const float up = __uint_as_float(uint32_t(127 + k) << 23);    // 2^k
+        const float down = __uint_as_float(uint32_t(127 - k) << 23);  // 2^-k
+        sscale = p.scale_log2 * down;
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            qa[st][0] = f16x2_of(x[4 * st] * up, x[4 * st + 1] * up);
+            qa[st][1] = f16x2_of(x[4 * st + 2] * up, x[4 * st + 3] * up);
+        }
+    }
+
+    // this lane's byte offsets within a chunk's first row of head g
+    const int offk0 = gq * row_elems + g * D + 32 * tq, offk1 = offk0 + 8 * row_elems;
+    const int offv = g * D + 16 * gq;
+
+    float o[8][4];  // O^T: block mb holds dims 16 gq + mb (o[mb][0..1]) and 16 gq + 8 + mb (o[mb][2..3])
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+    float m = -INFINITY, l = 0.f;  // head gq
+
+    for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
+        const int32_t phys = table[cb / p.block_size];
+        if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+            if (lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            continue;
+        }
+        // a chunk never crosses a block: cb and block_size are multiples of 16
+        const int64_t base = (int64_t(phys) * p.block_size + (cb % p.block_size)) * row_elems;
+        const int nvalid = t1 - cb;
+        if (PREFETCH_CHUNKS_FP8 > 0 && g == 0 && lane == 0) prefetch_chunk(cb + PREFETCH_CHUNKS_FP8 * wph * CHUNK);
+
+        uint4 kr[2][2], vr[4];
+        {
+            const uint8_t *k0 = kc + base + offk0, *k1 = kc + base + offk1;
+            const bool v0 = gq < nvalid, v1 = 8 + gq < nvalid;
+            kr[0][0] = v0 ? pa::ld_stream16(k0) : make_uint4(0, 0, 0, 0);
+            kr[0][1] = v0 ? pa::ld_stream16(k0 + 16) : make_uint4(0, 0, 0, 0);
+            kr[1][0] = v1 ? pa::ld_stream16(k1) : make_uint4(0, 0, 0, 0);
+            kr[1][1] = v1 ? pa::ld_stream16(k1 + 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int tok = 2 * tq + (i & 1) + 8 * (i >> 1);
+            vr[i] = tok < nvalid ? pa::ld_stream16(vc + base + tok * row_elems + offv) : make_uint4(0, 0, 0, 0);
+        }
+
+        float sc[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+            const uint32_t w[8] = {kr[nb][0].x, kr[nb][0].y, kr[nb][0].z, kr[nb][0].w,
+                                   kr[nb][1].x, kr[nb][1].y, kr[nb][1].z, kr[nb][1].w};
+            sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+#pragma unroll
+            for (int st = 0; st < 8; ++st)
+                mma_16816(sc[nb], qa[st][0], 0u, qa[st][1], 0u, e4m3x2_to_f16x2(w[st]), e4m3x2_to_f16x2(w[st] >> 16));
+        }
+
+        float x[4];
+        x[0] = 2 * tq < nvalid ? sc[0][0] * sscale : -INFINITY;
+        x[1] = 2 * tq + 1 < nvalid ? sc[0][1] * sscale : -INFINITY;
+        x[2] = 8 + 2 * tq < nvalid ? sc[1][0] * sscale : -INFINITY;
+        x[3] = 9 + 2 * tq < nvalid ? sc[1][1] * sscale : -INFINITY;
+        float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 1));
+        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 2));
+        // (finite: token 0 of a chunk is always in the split)
+        const bool need = cm > m + FP8_RESCALE_THRESHOLD;
+        if (__any_sync(FULL, need)) {
+            const float m_new = need ? cm : m;
+            const float alpha = pa::sm100::ex2_approx(m - m_new);  // 0 for the first chunk
+            l *= alpha;
+            m = m_new;
+            // the O^T columns of this lane are heads 2tq and 2tq + 1
+            const float a0 = __shfl_sync(FULL, alpha, 8 * tq), a1 = __shfl_sync(FULL, alpha, 8 * tq + 4);
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+                o[mb][0] *= a0;
+                o[mb][1] *= a1;
+                o[mb][2] *= a0;
+                o[mb][3] *= a1;
+            }
+        }
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = pa::sm100::ex2_approx(x[i] - m);
+        float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        ps += __shfl_xor_sync(FULL, ps, 1);
+        ps += __shfl_xor_sync(FULL, ps, 2);
+        l += ps;
+        const uint32_t pb0 = f16x2_of(pr[0], pr[1]), pb1 = f16x2_of(pr[2], pr[3]);
+        const uint32_t va[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w}, vb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t vcw[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, vd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                // bytes 2hb, 2hb+1 of word i (dims 4i + 2hb + {0,1} of the lane's 16) of
+                // two tokens, interleaved: (token a, token b) pairs for two dims
+                const uint32_t sel = hb ? 0x7362u : 0x5140u;
+                const uint32_t r0 = __byte_perm(va[i], vb[i], sel);       // dim slot gq, tokens 2tq, 2tq+1
+                const uint32_t r1 = __byte_perm(va[i + 2], vb[i + 2], sel);  // slot gq + 8
+                const uint32_t r2 = __byte_perm(vcw[i], vd[i], sel);      // slot gq, tokens 2tq+8, 2tq+9
+                const uint32_t r3 = __byte_perm(vcw[i + 2], vd[i + 2], sel);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int sh = 16 * jj;
+                    mma_16816(o[4 * i + 2 * hb + jj], e4m3x2_to_f16x2(r0 >> sh), e4m3x2_to_f16x2(r1 >> sh),
+                              e4m3x2_to_f16x2(r2 >> sh), e4m3x2_to_f16x2(r3 >> sh), pb0, pb1);
+                }
+            }
+        }
+    }
+
+    // this CTA's loads are done: the next kernel (the merge) may start launching
+    pa::grid_dependents_launch();
+
+    // every warp's partial through shared memory (the ring's space, once every
+    // warp's copies are done); warp g (sub 0) combines the warps of KV head g
+    __shared__ float red_o[NW][G][D];
+    __shared__ float red_ml[NW][G][2];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int h = 2 * tq + (cc & 1);
+            if (h < G) red_o[warp][h][16 * gq + 8 * (cc >> 1) + mb] = o[mb][cc];
+        }
+    if (tq == 0 && gq < G) {
+        red_ml[warp][gq][0] = m;
+        red_ml[warp][gq][1] = l;
+    }
+    __syncthreads();
+    if (sub != 0 || lane >= 16) return;
+    const int c = lane;  // dims 8c .. 8c + 7 of every head of the group
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float mm = -INFINITY;
+        for (int w = 0; w < wph; ++w) mm = fmaxf(mm, red_ml[g + w * p.kv_heads][h][0]);
+        float ll = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < wph; ++w) {
+            const int ww = g + w * p.kv_heads;
+            const float mw = red_ml[ww][h][0];
+            const float aw = (mw == -INFINITY) ? 0.f : exp2f(mw - mm);
+            ll += red_ml[ww][h][1] * aw;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(red_o[ww][h][8 * c + e], aw, acc[e]);
+        }
+        if (nsplit == 1) {
+            const float inv = p.out_scale / ll;
+            uint4 u;
+            u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + g * G + h) * D + 8 * c) = u;
+        } else {
+            const int64_t row = (int64_t(b) * p.max_splits + s) * p.num_heads + g * G + h;
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + row * D + 8 * c);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (c == 0) p.ws_ml[row] = make_float2(mm, ll);
+        }
+    }
+}
+
 // Merge the split partials of every sequence that has more than one split
 // ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
 // L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.  A thread per
@@ -649,13 +893,17 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 }
 
 template <int G, bool FP8>
-void launch_split(const DecodeParams &p, cudaStream_t stream)
+pa_status launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
-    if (!FP8 && p.cos_sin != nullptr)
-        pa::launch_pdl(decode_split_kernel<G, FP8, !FP8>, grid, dim3(NW * 32), 0, stream, p);
-    else
-        pa::launch_pdl(decode_split_kernel<G, FP8, false>, grid, dim3(NW * 32), 0, stream, p);
+    if constexpr (FP8) {
+        pa::launch_pdl(decode_fp8_mma_kernel<G>, grid, dim3(NW * 32), 0, stream, p);
+    } else if (p.cos_sin != nullptr) {
+        pa::launch_pdl(decode_split_kernel<G, true>, grid, dim3(NW * 32), 0, stream, p);
+    } else {
+        pa::launch_pdl(decode_split_kernel<G, false>, grid, dim3(NW * 32), 0, stream, p);
+    }
+    return PA_OK;
 }
 
 pa_status check_args(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
@@ -742,21 +990,23 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_heads / num_kv_heads;
+    pa_status ls = PA_OK;
     if (fp8) {
         switch (group) {
-        case 1: launch_split<1, true>(p, s); break;
-        case 2: launch_split<2, true>(p, s); break;
-        case 4: launch_split<4, true>(p, s); break;
-        default: launch_split<8, true>(p, s); break;
+        case 1: ls = launch_split<1, true>(p, s); break;
+        case 2: ls = launch_split<2, true>(p, s); break;
+        case 4: ls = launch_split<4, true>(p, s); break;
+        default: ls = launch_split<8, true>(p, s); break;
         }
     } else {
         switch (group) {
-        case 1: launch_split<1, false>(p, s); break;
-        case 2: launch_split<2, false>(p, s); break;
-        case 4: launch_split<4, false>(p, s); break;
-        default: launch_split<8, false>(p, s); break;
+        case 1: ls = launch_split<1, false>(p, s); break;
+        case 2: ls = launch_split<2, false>(p, s); break;
+        case 4: ls = launch_split<4, false>(p, s); break;
+        default: ls = launch_split<8, false>(p, s); break;
         }
     }
+    if (ls != PA_OK) return ls;
     if (plan.max_splits > 1) pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs)), dim3(256), 0, s, p);
     return pa::launch_status();
 }

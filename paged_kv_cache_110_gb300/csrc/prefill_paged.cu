@@ -388,30 +388,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         if (lane == 0) tma_prefetch_desc(&p.qmap);
         int n = 0;      // items published
         int qdone = 0;  // Q tiles announced (a TMA load, or an arrival for an empty tile)
-        // The items are ranked 32 at a time (a lane each): window `win` of the
-        // item list, `vbase` valid items before it, `mine` this CTA's items of
-        // the window not yet published.
+        // The items are ranked 32 groups at a time (a lane each).  A group is the
+        // items sharing (step, sequence), which are valid or not together: the
+        // `units` head pairs of one row tile (one item each when the keys are not
+        // split), or a single item when they are (the key splits of an item can
+        // differ) or when there would be more than 32 in a group.  Window `win`
+        // of the groups, `vbase` valid items before it; each lane keeps the mask
+        // of its group's items this CTA takes, consumed lane by lane in order.
+        const int per_group = (SPLIT || p.units > 32) ? 1 : p.units;
+        const int n_groups = n_items / per_group;
         int win = 0, vbase = 0;
-        uint32_t mine = 0;
+        uint32_t lane_mask = 0, lanes_left = 0, cur_bits = 0;
+        int cur_group = 0;
         while (true) {
             int w = -1;
-            while (mine == 0 && win < n_items) {
-                const int u = win + lane;
-                bool v = false;
-                if (u < n_items) {
-                    const Item it = decode_item<SPLIT>(p, u);
-                    v = it.valid;
+            while (true) {
+                if (cur_bits != 0) {
+                    w = cur_group * per_group + __ffs(cur_bits) - 1;
+                    cur_bits &= cur_bits - 1u;
+                    break;
+                }
+                if (lanes_left != 0) {
+                    const int l = __ffs(lanes_left) - 1;
+                    lanes_left &= lanes_left - 1u;
+                    cur_bits = __shfl_sync(FULL, lane_mask, l);
+                    cur_group = win - 32 + l;
+                    continue;
+                }
+                if (win >= n_groups) break;
+                const int gi = win + lane;
+                int cnt = 0;
+                if (gi < n_groups) {
+                    const Item it = decode_item<SPLIT>(p, gi * per_group);
+                    cnt = it.valid ? per_group : 0;
                     if (it.bad) pa::report(p.status, it.bad_code);
                 }
-                const uint32_t vm = __ballot_sync(FULL, v);
-                const int r = vbase + __popc(vm & ((1u << lane) - 1u));
-                mine = __ballot_sync(FULL, v && owner_of(r, int(gridDim.x)) == int(blockIdx.x));
-                vbase += __popc(vm);
+                int incl = cnt;  // inclusive prefix sum over the lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const int first = vbase + incl - cnt;
+                lane_mask = 0;
+                for (int e = 0; e < cnt; ++e)
+                    if (owner_of(first + e, int(gridDim.x)) == int(blockIdx.x)) lane_mask |= 1u << e;
+                lanes_left = __ballot_sync(FULL, lane_mask != 0);
+                vbase += __shfl_sync(FULL, incl, 31);
                 win += 32;
-            }
-            if (mine != 0) {
-                w = win - 32 + __ffs(mine) - 1;
-                mine &= mine - 1u;
             }
             const int slot = n % RING, tb = n & 1;
             if (n >= RING &&
@@ -655,6 +679,77 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         const float sl2 = p.scale_log2;
         int c = 0, no = 0, t = 0;  // tiles of this query tile, items with work, K/V tiles of all items
         bool ok = true;
+        // The epilogue of an item is deferred: its O stays in TMEM until this
+        // warpgroup has written the next item's first P, and is read just before
+        // that P is released to the MMA warp (the item's first P.V overwrites O).
+        // The wait for the last P.V and the normalise-and-store then overlap the
+        // next item's MMAs instead of holding them up.
+        bool pend = false;  // an item's O waits in TMEM
+        bool pe_split = false;
+        int pe_w = 0, pe_rows = 0, pe_tok = 0, pe_h = 0;
+        float pe_m = 0.f, pe_l = 0.f;
+        auto finish = [&](bool release_p) {
+            pend = false;
+            ok = __all_sync(FULL, mbar_wait(bar(B_OF + a), uint32_t(no) & 1u, abort_flag, p.wait_limit));
+            ++no;
+            if (!ok) return;
+            tc_fence_after();
+            auto release = [&]() {
+                tc_fence_before();
+                mbar_arrive(bar(B_PL + a));
+                mbar_arrive(bar(B_PF + a));
+            };
+            if (SPLIT && pe_split) {
+                // a share of a split item: unnormalised O and (max, sum) for the merge
+                const int64_t row = (int64_t(pe_w) * QT + a) * BM + r;
+                float *dst = p.ws_o + row * D;  // 256-byte aligned rows
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t o[64];
+                    tmem_ld64_sync(ocol + 64 * hh, o);
+                    if (release_p && hh == 1) release();
+                    if (r < pe_rows) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w8[e] = o[8 * v + e];
+                            st_global_v8(dst + 64 * hh + 8 * v, w8);
+                        }
+                    }
+                }
+                if (r < pe_rows) p.ws_ml[row] = make_float2(pe_m, pe_l);
+                return;
+            }
+            // O / l, packed to bf16 pairs as it is read (half the registers of
+            // the fp32 row: this runs inside the next item's tile loop)
+            const float inv = r < pe_rows ? 1.f / pe_l : 0.f;
+            uint32_t ob[64];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t o[64];
+                tmem_ld64_sync(ocol + 64 * hh, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    ob[32 * hh + i] = pa::pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            }
+            if (release_p) release();
+            if (r >= pe_rows) return;
+            uint16_t *dst = p.out + (int64_t(pe_tok + r) * p.num_heads + pe_h) * D;
+            if (p.out_v8) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    uint32_t w8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w8[e] = ob[8 * v + e];
+                    st_global_v8(dst + 16 * v, w8);
+                }
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) d4[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
+            }
+        };
         for (int n = 0;; ++n) {
             Item it;
             const int w = read_ring(n, it);
@@ -747,67 +842,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
                                 tmem_st32_sync(ocol + cc * 32, o);
                             }
                         }
-                        tc_fence_before();
-                        mbar_arrive(bar(B_PL + a));
+                        if (j > 0 || !pend) {
+                            tc_fence_before();
+                            mbar_arrive(bar(B_PL + a));
+                        }
                     }
                 }
                 l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-                tc_fence_before();
-                mbar_arrive(bar(B_PF + a));
+                if (j == 0 && pend) {
+                    finish(true);  // the previous item's epilogue, then this P is released
+                    if (!ok) break;
+                } else {
+                    tc_fence_before();
+                    mbar_arrive(bar(B_PF + a));
+                }
             }
             if (!ok) break;
-            // epilogue: the item's O of this query tile is complete once its barrier
-            // fires; the next item's first P.V (which overwrites O) waits for this
-            // warpgroup's next P, written after these reads
-            ok = __all_sync(FULL, mbar_wait(bar(B_OF + a), uint32_t(no) & 1u, abort_flag, p.wait_limit));
-            ++no;
-            if (!ok) break;
-            tc_fence_after();
-            // the whole O row in one TMEM load (one wait, not one per half)
-            uint32_t o[128];
-            tmem_ld128_sync(ocol, o);
-            if (SPLIT && it.split) {
-                // a share of a split item: unnormalised O and (max, sum) for the merge
-                if (r < it.rows[a]) {
-                    const int64_t row = (int64_t(w) * QT + a) * BM + r;
-                    float *dst = p.ws_o + row * D;  // 256-byte aligned rows
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        uint32_t w8[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w8[e] = o[8 * v + e];
-                        st_global_v8(dst + 8 * v, w8);
-                    }
-                    p.ws_ml[row] = make_float2(m_used, l);
-                }
-                continue;
-            }
-            if (r >= it.rows[a]) continue;
-            const float inv = 1.f / l;
-            uint16_t *dst = p.out + (int64_t(it.q0 + it.m0[a] + r) * p.num_heads + it.h[a]) * D;
-            if (p.out_v8) {
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    uint32_t w8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w8[e] = pa::pack_bf16x2(__uint_as_float(o[16 * v + 2 * e]) * inv,
-                                                __uint_as_float(o[16 * v + 2 * e + 1]) * inv);
-                    st_global_v8(dst + 16 * v, w8);
-                }
-            } else {
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    uint4 u;
-                    u.x = pa::pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                    u.y = pa::pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                    u.z = pa::pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                    u.w = pa::pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                    d4[v] = u;
-                }
-            }
+            pend = true;
+            pe_split = SPLIT && it.split;
+            pe_w = w;
+            pe_rows = it.rows[a];
+            pe_tok = it.q0 + it.m0[a];
+            pe_h = it.h[a];
+            pe_m = m_used;
+            pe_l = l;
         }
+        if (ok && pend) finish(false);
     }
 
     tc_fence_before();

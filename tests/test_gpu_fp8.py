@@ -72,21 +72,22 @@ def test_fp8_store_saturates_and_reports_bad_slots():
     assert ((codes & 0x7F) == 0x7E).mean() > 0.9
 
 
-def _decode_case(batch, k_scale, v_scale, ctx=None):
+def _decode_case(batch, k_scale, v_scale, ctx=None, q=None):
     d = dev()
     hist = wl.history_rows(batch.layout, batch.context_lens - batch.query_lens)
     ctx = batch.context_lens if ctx is None else np.asarray(ctx, np.int32)
+    q = batch.tokens.q if q is None else q
     gk, gv, ok, ov = _fp8_pools(batch, k_scale, v_scale, hist)
     max_ctx = int(ctx.max())
-    b = len(ctx)
-    ws = torch.empty(max(pa().pa_decode_workspace_bytes(b, 16, 128, max_ctx), 256), dtype=torch.uint8, device=d)
-    out = torch.full((b, 16, 128), float("nan"), dtype=torch.bfloat16, device=d)
+    b, hq = len(ctx), batch.num_heads
+    ws = torch.empty(max(pa().pa_decode_workspace_bytes(b, hq, 128, max_ctx), 256), dtype=torch.uint8, device=d)
+    out = torch.full((b, hq, 128), float("nan"), dtype=torch.bfloat16, device=d)
     st = Status(d)
-    pa().pa_decode_paged_fp8(batch.tokens.q, gk, gv, k_scale, v_scale, i32(batch.block_tables, d), i32(ctx, d),
+    pa().pa_decode_paged_fp8(q, gk, gv, k_scale, v_scale, i32(batch.block_tables, d), i32(ctx, d),
                              max_ctx, batch.scale, out, ws, dev_status=st.t)
     torch.cuda.synchronize()
     assert int(st.t.item()) == 0
-    q_bits = wl.bf16_bits(batch.tokens.q)
+    q_bits = wl.bf16_bits(q)
     ref = oracle.decode_fp8(q_bits, ok, ov, k_scale, v_scale, batch.block_tables, ctx, batch.scale)
     return out, ref, hist
 
@@ -106,6 +107,29 @@ def test_fp8_decode_block_size_16_and_padding_rows():
     out, ref, _ = _decode_case(batch, 2.0 ** -6, 2.0 ** -6, ctx=ctx)
     assert_close(out, ref, "fp8 decode bs 16")
     assert (out[[1, 5]].float() == 0).all()
+
+
+# one sequence of a single token, ragged chunk tails, exact chunks, several
+# splits (merged) and a long one; every group size the kernel has (G = 1, 2,
+# 4, 8 query heads per KV head, one to eight warps per KV head)
+@pytest.mark.parametrize("hq,hkv,bs", [(8, 8, 16), (16, 4, 64), (32, 4, 256), (8, 1, 32), (4, 2, 48)])
+def test_fp8_decode_head_layouts(hq, hkv, bs):
+    live = np.array([1, 15, 16, 17, 100, 700, 2100, 33])
+    batch = wl.paged_batch(wl.SEED_BASE + 85 + hq + 3 * hkv, live, np.ones_like(live), bs, num_heads=hq,
+                           num_kv_heads=hkv, device=dev())
+    out, ref, _ = _decode_case(batch, 2.0 ** -6, 2.0 ** -5)
+    assert_close(out, ref, f"fp8 decode hq={hq} hkv={hkv} bs={bs}")
+
+
+# queries far from unit size: a bf16 query of any normal magnitude enters the
+# MMA exactly (scaled by a power of two per head, undone on the score)
+@pytest.mark.parametrize("qmul", [2.0 ** 12, 2.0 ** -12])
+def test_fp8_decode_query_magnitudes(qmul):
+    live = np.array([300, 40, 1000, 17])
+    batch = wl.paged_batch(wl.SEED_BASE + 86, live, np.ones_like(live), 16, device=dev())
+    q = (batch.tokens.q.float() * qmul).to(torch.bfloat16)
+    out, ref, _ = _decode_case(batch, 2.0 ** -6, 2.0 ** -6, q=q)
+    assert_close(out, ref, f"fp8 decode, queries x {qmul}")
 
 
 def test_fp8_effect_against_the_bf16_oracle():
