@@ -267,7 +267,13 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
  * Sequence b attends with q[b] to keys 0 .. context_lens[b]-1 read through
  * block_table[b] (context_lens counts the token written this step).
  * Softmax statistics of key ranges ("splits") are merged exactly as in §9.5
- * (maximum, exponent sum, weighted numerator), never per page.
+ * (maximum, exponent sum, weighted numerator), never per page: through the
+ * workspace and a merge kernel, or, for long contexts in a large batch (the
+ * bf16 calls whose split plan would exceed eight splits, with
+ * max_context_len <= 8192 and at least four cluster CTAs per SM), inside one
+ * thread-block cluster per sequence (eight equal splits, merged in
+ * distributed shared memory), which leaves the workspace untouched.  Either
+ * way the caller passes a workspace of the size below.
  *
  *   q             [num_seqs, num_heads, head_dim] bf16, seq stride
  *                 q_stride_seq elements.

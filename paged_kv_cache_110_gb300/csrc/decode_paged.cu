@@ -233,7 +233,7 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-template <int G, bool ROPE>
+template <int G, bool ROPE, bool CLUSTER>
 __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
 {
     using KV = KvRow;
@@ -259,14 +259,21 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
         return;
     }
-    const int nsplit = (ctx + p.split_len - 1) / p.split_len;
-    if (s >= nsplit) return;
+    // In a cluster the sequence's keys are cut into as many equal splits (whole
+    // 16-token chunks) as the cluster has CTAs, so that its CTAs finish
+    // together; otherwise every sequence uses the call's split length.
+    const int split_len = CLUSTER ? ((ctx + int(gridDim.y) - 1) / int(gridDim.y) + CHUNK - 1) / CHUNK * CHUNK
+                                  : p.split_len;
+    const int nsplit = (ctx + split_len - 1) / split_len;
+    // (in a cluster every CTA stays to the end: it takes part in the merge's
+    // barriers; a CTA past the sequence's splits reads nothing)
+    if (!CLUSTER && s >= nsplit) return;
 
     const int g = warp % p.kv_heads;
     const int sub = warp / p.kv_heads;
     const int wph = NW / p.kv_heads;
-    const int t0 = s * p.split_len;
-    const int t1 = min(ctx, t0 + p.split_len);
+    const int t0 = s * split_len;
+    const int t1 = min(ctx, t0 + split_len);
     const int64_t row_elems = int64_t(p.kv_heads) * D;
     const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
 
@@ -473,8 +480,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(FULL, o[h][e], 16);
 
     // warps that shared one KV head (Hkv < 8) merge through shared memory
-    __shared__ float red_o[NW][G][D];
-    __shared__ float red_ml[NW][G][2];
+    __shared__ __align__(16) float red_o[NW][G][D];
+    __shared__ __align__(16) float red_ml[NW][G][2];
     if (wph > 1) {
         if (lane < 16) {
 #pragma unroll
@@ -490,9 +497,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
             }
         }
         __syncthreads();
-        if (sub != 0) return;
+        if (!CLUSTER && sub != 0) return;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
+            if (sub != 0) break;
             float mm = m[h];
             for (int w = 1; w < wph; ++w) mm = fmaxf(mm, red_ml[g + w * p.kv_heads][h][0]);
             const float a0 = exp2f(m[h] - mm);
@@ -510,6 +518,84 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
             m[h] = mm;
             l[h] = ll;
         }
+    }
+
+    if constexpr (CLUSTER) {
+        // The splits of this sequence are the CTAs of one cluster (its rank = s).
+        // Each leaves its partial (max, sum, unnormalised O of every head of the
+        // sequence) in its own shared memory, in red_o / red_ml's space: head row
+        // g * G + h is the row warp g's own partial occupied, and the other
+        // warps' rows it read lie past num_heads, so no warp overwrites a row
+        // another still reads.  After a cluster barrier, CTA s merges heads
+        // s, s + nsplit, ... reading every split's partial through distributed
+        // shared memory (the same rule as the merge kernel), and a second
+        // barrier keeps every CTA's shared memory alive until all have read it.
+        // Every thread of every CTA reaches both barriers.
+        float *xo = &red_o[0][0][0];                                  // [num_heads][D]
+        float2 *xm = reinterpret_cast<float2 *>(&red_ml[0][0][0]);   // [num_heads]
+        const bool lead = sub == 0 && lane < 16;
+        __syncwarp();  // (the merge above read this warp's rows of red_ml)
+        if (lead && s < nsplit) {  // (a CTA past the sequence's splits holds no partial)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const int hr = g * G + h;
+                if (nsplit == 1) {
+                    const float inv = p.out_scale / l[h];
+                    uint4 u;
+                    u.x = pa::pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
+                    u.y = pa::pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
+                    u.z = pa::pack_bf16x2(o[h][4] * inv, o[h][5] * inv);
+                    u.w = pa::pack_bf16x2(o[h][6] * inv, o[h][7] * inv);
+                    *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + hr) * D + 8 * c) = u;
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(xo + hr * D + 8 * c);
+                    dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+                    dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+                    if (c == 0) xm[hr] = make_float2(m[h], l[h]);
+                }
+            }
+        }
+        pa::sm100::cluster_sync();
+        if (nsplit > 1 && s < nsplit) {
+            const int mine = (p.num_heads - s + nsplit - 1) / nsplit;  // heads s, s + nsplit, ...
+            for (int it = threadIdx.x; it < mine * 16; it += NW * 32) {
+                const int h = s + (it >> 4) * nsplit, c8 = (it & 15) * 8;
+                const uint32_t ao = pa::sm100::smem_u32(xo + h * D + c8), am = pa::sm100::smem_u32(xm + h);
+                float2 ml[NW];
+                float4 x0[NW], x1[NW];
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    if (j < nsplit) {
+                        ml[j] = pa::sm100::ld_shared_cluster_v2(pa::sm100::mapa_shared(am, j));
+                        x0[j] = pa::sm100::ld_shared_cluster_v4(pa::sm100::mapa_shared(ao, j));
+                        x1[j] = pa::sm100::ld_shared_cluster_v4(pa::sm100::mapa_shared(ao + 16, j));
+                    } else {
+                        ml[j] = make_float2(-INFINITY, 0.f);
+                        x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float mm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < NW; ++j) mm = fmaxf(mm, ml[j].x);
+                float ll = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    const float w = (ml[j].x == -INFINITY) ? 0.f : exp2f(ml[j].x - mm);
+                    ll += ml[j].y * w;
+                    acc[0] += x0[j].x * w; acc[1] += x0[j].y * w; acc[2] += x0[j].z * w; acc[3] += x0[j].w * w;
+                    acc[4] += x1[j].x * w; acc[5] += x1[j].y * w; acc[6] += x1[j].z * w; acc[7] += x1[j].w * w;
+                }
+                const float inv = p.out_scale / ll;
+                uint4 u;
+                u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+                u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + h) * D + c8) = u;
+            }
+        }
+        pa::sm100::cluster_sync();
+        return;
     }
 
     if (lane >= 16) return;
@@ -778,8 +864,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
     // this CTA's loads are done: the next kernel (the merge) may start launching
     pa::grid_dependents_launch();
 
-    // every warp's partial through shared memory (the ring's space, once every
-    // warp's copies are done); warp g (sub 0) combines the warps of KV head g
+    // every warp's partial through shared memory; warp g (sub 0) combines the
+    // warps of KV head g
     __shared__ float red_o[NW][G][D];
     __shared__ float red_ml[NW][G][2];
 #pragma unroll
@@ -892,16 +978,43 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     }
 }
 
-template <int G, bool FP8>
-pa_status launch_split(const DecodeParams &p, cudaStream_t stream)
+// Long contexts in a large batch: every sequence is split into CLUSTER_SPLITS
+// equal parts, launched as one thread-block cluster that merges them in
+// distributed shared memory (the workspace and the merge kernel go unused).
+// Taken where the split plan would cut sequences into more parts than that,
+// the batch has at least four such CTAs per SM and no part exceeds
+// CLUSTER_MAX_SPLIT tokens (measured: a 512 x U[1k, 4k] batch 3% faster than
+// 256-token splits and the merge kernel; shorter contexts, where the plan's
+// 128-token splits leave many sequences with fewer parts than a cluster has
+// CTAs, were slower in clusters).
+constexpr int CLUSTER_SPLITS = 8;
+constexpr int CLUSTER_MAX_SPLIT = 1024;
+inline bool use_cluster(bool fp8, int num_seqs, int max_ctx, const Plan &plan)
 {
-    const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
+    const int sms = pa::num_sms() > 0 ? pa::num_sms() : 152;
+    return !fp8 && plan.max_splits > CLUSTER_SPLITS && max_ctx <= CLUSTER_SPLITS * CLUSTER_MAX_SPLIT &&
+           int64_t(num_seqs) * CLUSTER_SPLITS >= 4LL * sms;
+}
+
+template <int G, bool FP8>
+pa_status launch_split(const DecodeParams &p, bool cluster, cudaStream_t stream)
+{
+    const dim3 block(NW * 32);
     if constexpr (FP8) {
-        pa::launch_pdl(decode_fp8_mma_kernel<G>, grid, dim3(NW * 32), 0, stream, p);
-    } else if (p.cos_sin != nullptr) {
-        pa::launch_pdl(decode_split_kernel<G, true>, grid, dim3(NW * 32), 0, stream, p);
+        const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
+        pa::launch_pdl(decode_fp8_mma_kernel<G>, grid, block, 0, stream, p);
+    } else if (cluster) {
+        const dim3 grid(unsigned(p.num_seqs), unsigned(CLUSTER_SPLITS));
+        if (p.cos_sin != nullptr)
+            pa::launch_pdl_cluster_y(decode_split_kernel<G, true, true>, grid, block, 0, stream, CLUSTER_SPLITS, p);
+        else
+            pa::launch_pdl_cluster_y(decode_split_kernel<G, false, true>, grid, block, 0, stream, CLUSTER_SPLITS, p);
     } else {
-        pa::launch_pdl(decode_split_kernel<G, false>, grid, dim3(NW * 32), 0, stream, p);
+        const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
+        if (p.cos_sin != nullptr)
+            pa::launch_pdl(decode_split_kernel<G, true, false>, grid, block, 0, stream, p);
+        else
+            pa::launch_pdl(decode_split_kernel<G, false, false>, grid, block, 0, stream, p);
     }
     return PA_OK;
 }
@@ -990,24 +1103,26 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_heads / num_kv_heads;
+    const bool cl = use_cluster(fp8, num_seqs, max_context_len, plan);
     pa_status ls = PA_OK;
     if (fp8) {
         switch (group) {
-        case 1: ls = launch_split<1, true>(p, s); break;
-        case 2: ls = launch_split<2, true>(p, s); break;
-        case 4: ls = launch_split<4, true>(p, s); break;
-        default: ls = launch_split<8, true>(p, s); break;
+        case 1: ls = launch_split<1, true>(p, false, s); break;
+        case 2: ls = launch_split<2, true>(p, false, s); break;
+        case 4: ls = launch_split<4, true>(p, false, s); break;
+        default: ls = launch_split<8, true>(p, false, s); break;
         }
     } else {
         switch (group) {
-        case 1: ls = launch_split<1, false>(p, s); break;
-        case 2: ls = launch_split<2, false>(p, s); break;
-        case 4: ls = launch_split<4, false>(p, s); break;
-        default: ls = launch_split<8, false>(p, s); break;
+        case 1: ls = launch_split<1, false>(p, cl, s); break;
+        case 2: ls = launch_split<2, false>(p, cl, s); break;
+        case 4: ls = launch_split<4, false>(p, cl, s); break;
+        default: ls = launch_split<8, false>(p, cl, s); break;
         }
     }
     if (ls != PA_OK) return ls;
-    if (plan.max_splits > 1) pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs)), dim3(256), 0, s, p);
+    if (plan.max_splits > 1 && !cl)
+        pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs)), dim3(256), 0, s, p);
     return pa::launch_status();
 }
 

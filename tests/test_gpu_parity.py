@@ -323,6 +323,27 @@ def test_decode_shapes(hq, hkv, bs):
     _decode_vs_oracle(batch)
 
 
+# Long contexts in a batch large enough that every sequence is split over the
+# eight CTAs of one thread-block cluster and merged in distributed shared
+# memory: sequences of one token, ragged and exact chunks, sequences with fewer
+# splits than the cluster has CTAs, and long ones, for every group size; then
+# the fused KV write + decode over the same cluster path, bit-equal to the two
+# calls.
+@pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 256), (8, 1, 64), (32, 4, 16), (4, 2, 48)])
+def test_decode_cluster_merge(hq, hkv, bs):
+    ctx = np.resize(np.array([1, 15, 16, 17, 100, 129, 255, 256, 1000, 2100, 4000, 33]), 96)
+    batch = wl.paged_batch(520 + hq + bs, ctx, np.ones_like(ctx), bs, num_heads=hq, num_kv_heads=hkv,
+                           device=dev())
+    out, kc, vc = _decode_vs_oracle(batch, seqs=list(range(12)) + [50, 95])
+    kf, vf = batch.k_cache.clone(), batch.v_cache.clone()
+    st = Status(kf.device)
+    fused = _store_decode_fused(batch.tokens.q, batch.tokens.k, batch.tokens.v, kf, vf, batch.block_tables,
+                                batch.context_lens, batch.scale, st)
+    assert st.value() == 0
+    assert torch.equal(fused.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(kf.view(torch.int16), kc.view(torch.int16)) and torch.equal(vf.view(torch.int16), vc.view(torch.int16))
+
+
 def _store_decode_fused(q, k_new, v_new, kc, vc, tables, ctx, scale, status, max_ctx=None):
     d = kc.device
     b = q.shape[0]
