@@ -303,8 +303,6 @@ __device__ __forceinline__ void mask_tail(uint32_t (&s)[N], int base, int limit)
 template <bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
-    // launched programmatically: the KV write before it must be complete
-    pa::grid_dependency_wait();
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
@@ -361,6 +359,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // launched programmatically: the setup above (barriers, tensor memory) may
+    // overlap the kernel before; everything below may read what it wrote (the
+    // KV write of this step's tokens)
+    pa::grid_dependency_wait();
     // the softmax warpgroups hold a 64-column slice of S, its P and O rows in
     // registers; the scheduler, producer and MMA warps need few
     static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= 168 * NTHREADS, "register split");
