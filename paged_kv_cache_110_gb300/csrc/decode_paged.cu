@@ -60,7 +60,7 @@ struct DecodeParams {
     int num_heads;
     int kv_heads;
     float scale_log2;   // scale * log2(e) (times the K scale for fp8 pools)
-    float out_scale;    // 1, or the V scale for fp8 pools
+    float out_scale;    // 1, or the V scale times 2^8 for fp8 pools (their values enter the MMAs times 2^-8)
     uint16_t *out;
     const uint16_t *k_new;  // fused KV write: the step's new K / V rows [num_seqs][kv_heads][D], or null
     const uint16_t *v_new;
@@ -628,10 +628,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 //
 // Converting every E4M3 code to f32 for CUDA-core FMAs costs more instruction
 // issue than the byte is worth, so fp8 pools would leave HBM idle that way.
-// Here one conversion instruction turns two codes into an f16 pair (exact:
-// every E4M3 value is an f16 value) and the dot products and the P.V sums run
-// as MMAs; the K scale is folded into the score scale and the V scale into the
-// output, as for the CUDA-core path.  The work split is the bf16 kernel's:
+// Here the codes become f16 exactly (every E4M3 value, and that value times
+// 2^-8, is an f16 value): the keys four at a time by a byte permute and a
+// shift (times 2^-8, folded into the score scale and the output scale); the
+// dot products and the P.V sums run as MMAs.
+// The K scale is folded into the score scale and the V scale into the output.  The work split is the bf16 kernel's:
 // CTA = (sequence, split), warp = (KV head, every wph-th 16-token chunk).
 // Lane (gq, tq) = (lane / 4, lane % 4).  Per chunk:
 //   S = Q K^T   A = the group's G query heads (rows 0..G-1 of 16, f16; each
@@ -656,10 +657,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // the prescale gives); P (below 2^8) is rounded to f16 (relative 2^-11) for
 // the P.V MMA.
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+// The four E4M3 codes of w as two f16 pairs (codes 0, 1 and codes 2, 3), each
+// value times 2^-8, exactly: with the sign bits taken out, a byte permute puts
+// each code's seven low bits in the low byte of a 16-bit lane and its sign as
+// bit 0 of the lane's high byte; a shift left by 7 then moves eeee mmm to where
+// an f16 keeps the low four exponent bits and the top three mantissa bits
+// (the f16 exponent bias, 15, exceeds E4M3's, 7, by 8: the 2^-8; E4M3
+// subnormals land on f16 subnormals) and the sign to bit 15.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(two_codes & 0xffffu), __NV_E4M3);
-    return uint32_t(r.x) | (uint32_t(r.y) << 16);
+    const uint32_t mag = w & 0x7f7f7f7fu, sgn = (w >> 7) & 0x01010101u;
+    lo = __byte_perm(mag, sgn, 0x5140u) << 7;
+    hi = __byte_perm(mag, sgn, 0x7362u) << 7;
 }
 
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
@@ -751,7 +760,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
         if (mx > 0.f) k = min(126, max(-126, 13 - (int((__float_as_uint(mx) >> 23) & 0xffu) - 127)));
         const float up = __uint_as_float(uint32_t(127 + k) << 23);    // 2^k
         const float down = __uint_as_float(uint32_t(127 - k) << 23);  // 2^-k
-        sscale = p.scale_log2 * down;
+        sscale = p.scale_log2 * down * 256.f;  // (the keys enter the MMA times 2^-8)
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
             qa[st][0] = f16x2_of(x[4 * st] * up, x[4 * st + 1] * up);
@@ -801,8 +810,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
                                    kr[nb][1].x, kr[nb][1].y, kr[nb][1].z, kr[nb][1].w};
             sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
 #pragma unroll
-            for (int st = 0; st < 8; ++st)
-                mma_16816(sc[nb], qa[st][0], 0u, qa[st][1], 0u, e4m3x2_to_f16x2(w[st]), e4m3x2_to_f16x2(w[st] >> 16));
+            for (int st = 0; st < 8; ++st) {
+                uint32_t b0, b1;
+                e4m3x4_to_f16x2x2(w[st], b0, b1);
+                mma_16816(sc[nb], qa[st][0], 0u, qa[st][1], 0u, b0, b1);
+            }
         }
 
         float x[4];
@@ -845,18 +857,16 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 // bytes 2hb, 2hb+1 of word i (dims 4i + 2hb + {0,1} of the lane's 16) of
-                // two tokens, interleaved: (token a, token b) pairs for two dims
+                // two tokens a, b, interleaved (a d0, b d0, a d1, b d1): converted, the
+                // low f16 pair is dim d0's (a, b) and the high pair dim d1's
                 const uint32_t sel = hb ? 0x7362u : 0x5140u;
-                const uint32_t r0 = __byte_perm(va[i], vb[i], sel);       // dim slot gq, tokens 2tq, 2tq+1
-                const uint32_t r1 = __byte_perm(va[i + 2], vb[i + 2], sel);  // slot gq + 8
-                const uint32_t r2 = __byte_perm(vcw[i], vd[i], sel);      // slot gq, tokens 2tq+8, 2tq+9
-                const uint32_t r3 = __byte_perm(vcw[i + 2], vd[i + 2], sel);
+                uint32_t f0[2], f1[2], f2[2], f3[2];
+                e4m3x4_to_f16x2x2(__byte_perm(va[i], vb[i], sel), f0[0], f0[1]);          // dim slot gq, tokens 2tq, 2tq+1
+                e4m3x4_to_f16x2x2(__byte_perm(va[i + 2], vb[i + 2], sel), f1[0], f1[1]);  // slot gq + 8
+                e4m3x4_to_f16x2x2(__byte_perm(vcw[i], vd[i], sel), f2[0], f2[1]);         // slot gq, tokens 2tq+8, 2tq+9
+                e4m3x4_to_f16x2x2(__byte_perm(vcw[i + 2], vd[i + 2], sel), f3[0], f3[1]);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int sh = 16 * jj;
-                    mma_16816(o[4 * i + 2 * hb + jj], e4m3x2_to_f16x2(r0 >> sh), e4m3x2_to_f16x2(r1 >> sh),
-                              e4m3x2_to_f16x2(r2 >> sh), e4m3x2_to_f16x2(r3 >> sh), pb0, pb1);
-                }
+                for (int jj = 0; jj < 2; ++jj) mma_16816(o[4 * i + 2 * hb + jj], f0[jj], f1[jj], f2[jj], f3[jj], pb0, pb1);
             }
         }
     }
@@ -1082,7 +1092,7 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
     p.num_heads = num_heads;
     p.kv_heads = num_kv_heads;
     p.scale_log2 = scale * LOG2E * k_scale;
-    p.out_scale = v_scale;
+    p.out_scale = fp8 ? v_scale * 256.f : v_scale;  // (fp8 values enter the P.V MMAs times 2^-8)
     p.out = static_cast<uint16_t *>(out);
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
