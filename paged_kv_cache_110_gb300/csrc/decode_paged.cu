@@ -639,9 +639,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 //               head multiplied by the power of two that puts its largest
 //               magnitude in [2^13, 2^14), undone on the fp32 score), B = the
 //               keys of an 8-token block; two blocks x 8 steps of 16 dims.
-//               Lane (gq, tq) supplies token gq of a block, dims 32 tq ..
-//               32 tq + 31: each step takes the dims in an order of its own,
-//               the query the same, so that a lane reads 32 contiguous bytes.
+//               Lane (gq, tq) supplies token gq of a block, dims 16 tq .. + 15
+//               and 64 + 16 tq .. + 15: each step takes four of them (one
+//               word), the query the same, and the four lanes of a token read
+//               adjacent 16-byte pieces.
 //   softmax     the accumulator holds head gq's scores of tokens 2tq, 2tq+1
 //               and 8+2tq, 9+2tq: max and sum over the 4 lanes of head gq.
 //               The running max moves only when a score passes it by more than
@@ -733,17 +734,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
     };
     if (g == 0 && lane == 0) prefetch_chunk(t0 + sub * CHUNK);
 
-    // the query: head gq of the group (rows gq >= G stay zero), dims 32 tq .. 32 tq + 31
+    // the query: head gq of the group (rows gq >= G stay zero), the lane's key
+    // dims 16 tq .. + 15 (x[0..15]) and 64 + 16 tq .. + 15 (x[16..31])
     uint32_t qa[8][2];
     float sscale;  // score scale of head gq in log2 units, the prescale undone
     {
         float x[32];
         if (gq < G) {
-            const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + gq) * D + 32 * tq);
+            const uint16_t *qrow = p.q + int64_t(b) * p.q_stride + (g * G + gq) * D + 16 * tq;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float f[8];
-                unpack8(qp[i], f);
+                unpack8(*reinterpret_cast<const uint4 *>(qrow + 64 * (i >> 1) + 8 * (i & 1)), f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[8 * i + e] = f[e];
             }
@@ -768,8 +770,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
         }
     }
 
-    // this lane's byte offsets within a chunk's first row of head g
-    const int offk0 = gq * row_elems + g * D + 32 * tq, offk1 = offk0 + 8 * row_elems;
+    // this lane's byte offsets within a chunk's first row of head g: its two
+    // 16-byte pieces of a key row lie 64 bytes apart and the four lanes of a
+    // token hold adjacent pieces, so each load instruction reads whole 64-byte runs
+    const int offk0 = gq * row_elems + g * D + 16 * tq, offk1 = offk0 + 8 * row_elems;
     const int offv = g * D + 16 * gq;
 
     float o[8][4];  // O^T: block mb holds dims 16 gq + mb (o[mb][0..1]) and 16 gq + 8 + mb (o[mb][2..3])
@@ -793,9 +797,9 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
             const uint8_t *k0 = kc + base + offk0, *k1 = kc + base + offk1;
             const bool v0 = gq < nvalid, v1 = 8 + gq < nvalid;
             kr[0][0] = v0 ? pa::ld_stream16(k0) : make_uint4(0, 0, 0, 0);
-            kr[0][1] = v0 ? pa::ld_stream16(k0 + 16) : make_uint4(0, 0, 0, 0);
+            kr[0][1] = v0 ? pa::ld_stream16(k0 + 64) : make_uint4(0, 0, 0, 0);
             kr[1][0] = v1 ? pa::ld_stream16(k1) : make_uint4(0, 0, 0, 0);
-            kr[1][1] = v1 ? pa::ld_stream16(k1 + 16) : make_uint4(0, 0, 0, 0);
+            kr[1][1] = v1 ? pa::ld_stream16(k1 + 64) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -923,6 +927,296 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
     }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 decode for four or more query heads per KV head on the warp-level
+// tensor-core MMA (mma.sync m16n8k16, bf16 operands, f32 accumulators).
+//
+// The CUDA-core kernel keeps G x 8 partial dot products, G x 8 query values
+// and G x 8 outputs per lane; from G = 4 on they no longer fit its register
+// budget and spill.  Here S = Q K^T and O^T += V^T P^T run as MMAs laid out
+// as the fp8 kernel's (see there): lane (gq, tq) = (lane / 4, lane % 4)
+// supplies token gq of each 8-token block of a 16-token chunk, dims 32 j + 8 tq
+// .. + 7 for j < 4 (the pool's bf16 words are the B registers as they are, the
+// query taken in the same dim order; the four lanes of a token read adjacent
+// 16-byte pieces), and dims 8 gq .. + 7 and 64 + 8 gq .. + 7 of tokens 2tq,
+// 2tq+1, 2tq+8, 2tq+9 for P.V (two tokens' values of one dim paired by a byte
+// permute).  The query (with the head norm and RoPE when fused) is
+// formed in the half-warp layout of the CUDA-core kernel and staged through
+// shared memory into the A fragments.  P is rounded to bf16 for the P.V MMA.
+// The fused KV write, the split partials and the output are the CUDA-core
+// kernel's.
+
+// d += A (16 x 16, row) * B (16 x 8, col), bf16 in, f32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int G, bool ROPE>
+__global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const DecodeParams p)
+{
+    const int b = blockIdx.x, s = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int half = lane >> 4, c = lane & 15;
+    // launched programmatically: everything below may depend on the previous
+    // kernel (the KV write of this step's token)
+    pa::grid_dependency_wait();
+
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size ||
+        (ROPE && int64_t(ctx) > p.max_positions)) {
+        if (s == 0 && threadIdx.x == 0) pa::report(p.status, PA_ERR_BOUNDS);
+        ctx = 0;
+    }
+    if (ctx == 0) {  // padded row: output zeros, read nothing
+        if (s == 0) {
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + int64_t(b) * p.num_heads * D);
+            for (int i = threadIdx.x; i < p.num_heads * D / 8; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    const int nsplit = (ctx + p.split_len - 1) / p.split_len;
+    if (s >= nsplit) return;
+
+    const int g = warp % p.kv_heads;
+    const int sub = warp / p.kv_heads;
+    const int wph = NW / p.kv_heads;
+    const int t0 = s * p.split_len;
+    const int t1 = min(ctx, t0 + p.split_len);
+    const int row_elems = p.kv_heads * D;
+    const int32_t *table = p.block_table + int64_t(b) * p.max_blocks;
+    const uint16_t *kc = static_cast<const uint16_t *>(p.k_cache);
+    const uint16_t *vc = static_cast<const uint16_t *>(p.v_cache);
+
+    // Fused KV write, as in the CUDA-core kernel: the sequence's last split
+    // stores the step's new token (position ctx - 1) before any warp reads, and
+    // the chunk holding it is read through L2.
+    int new_tok = -1;
+    if (p.k_new != nullptr && s == nsplit - 1) {  // the same for the whole CTA
+        new_tok = ctx - 1;
+        if (sub == 0) {
+            const int32_t phys = table[new_tok / p.block_size];
+            const uint16_t *src = (half ? p.v_new : p.k_new) + int64_t(b) * p.kv_new_stride + g * D + 8 * c;
+            uint4 u = *reinterpret_cast<const uint4 *>(src);
+            if constexpr (ROPE) {
+                const RopeLane rl = rope_lane(p.k_weight, p.cos_sin + int64_t(new_tok) * D, c);
+                float x[8];
+                unpack8(u, x);
+                norm_rope_row8(x, c, p.k_weight != nullptr, rl.w, p.eps, rl.c, rl.s);
+                if (!half) u = pack8(x);
+            }
+            if (phys >= 0 && int64_t(phys) < p.num_blocks) {
+                const int64_t row = int64_t(phys) * p.block_size + new_tok % p.block_size;
+                uint16_t *dst = static_cast<uint16_t *>(const_cast<void *>(half ? p.v_cache : p.k_cache)) +
+                                row * row_elems + g * D + 8 * c;
+                *reinterpret_cast<uint4 *>(dst) = u;
+            }
+        }
+        __syncthreads();
+    }
+
+    auto prefetch_chunk = [&](int cf) {  // a chunk's 16 rows of all KV heads: one contiguous run of one block
+        if (cf >= t1) return;
+        const int32_t pf = table[cf / p.block_size];
+        if (pf < 0 || int64_t(pf) >= p.num_blocks) return;
+        const int64_t r = (int64_t(pf) * p.block_size + cf % p.block_size) * row_elems;
+        const uint32_t bytes = uint32_t(min(CHUNK, t1 - cf) * row_elems * 2);
+        const uint32_t b16 = (bytes + 15u) & ~15u;
+        pa::sm100::prefetch_l2_bulk(kc + r, b16);
+        pa::sm100::prefetch_l2_bulk(vc + r, b16);
+    };
+    if (g == 0 && lane == 0) prefetch_chunk(t0 + sub * CHUNK);
+
+    // the group's query heads, this warp's slice of the merge buffer as staging
+    __shared__ __align__(16) float red_o[NW][G][D];
+    __shared__ __align__(16) float red_ml[NW][G][2];
+    // (the A fragments are read from the staging at every chunk: per 16-dim step,
+    // head gq's dims 32 tq + 4 st + {0, 1} and + {2, 3}, one 8-byte load)
+    uint16_t *qs = reinterpret_cast<uint16_t *>(&red_o[warp][0][0]);  // [G][D] bf16
+    {
+        RopeLane rl;
+        if constexpr (ROPE) rl = rope_lane(p.q_weight, p.cos_sin + int64_t(ctx - 1) * D, c);
+#pragma unroll
+        for (int i = 0; i < (G + 1) / 2; ++i) {  // half-warp `half` takes heads half, half + 2, ...
+            const int h = 2 * i + half;
+            const bool hv = h < G;
+            uint4 u = hv ? *reinterpret_cast<const uint4 *>(p.q + int64_t(b) * p.q_stride + (g * G + h) * D + 8 * c)
+                         : make_uint4(0, 0, 0, 0);
+            if constexpr (ROPE) {
+                float x[8];
+                unpack8(u, x);
+                norm_rope_row8(x, c, p.q_weight != nullptr, rl.w, p.eps, rl.c, rl.s);
+                u = pack8(x);
+            }
+            if (hv) *reinterpret_cast<uint4 *>(qs + h * D + 8 * c) = u;
+        }
+        __syncwarp();
+    }
+    const uint16_t *qrow = qs + (gq < G ? gq : 0) * D + 8 * tq;
+
+    // this lane's element offsets within a chunk's first row: its four 8-dim
+    // pieces of a key row are 32 dims apart and the four lanes of a token hold
+    // adjacent pieces, so that each load instruction reads whole 64-byte runs
+    // (K); its two pieces of a value row, 64 dims apart, likewise (V)
+    const int offk0 = gq * row_elems + g * D + 8 * tq, offk1 = offk0 + 8 * row_elems;
+    const int offv = g * D + 8 * gq;
+
+    float o[8][4];  // O^T: block mb holds dims 8 gq + mb (o[mb][0..1]) and 64 + 8 gq + mb (o[mb][2..3])
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+    float m = -INFINITY, l = 0.f;  // head gq
+    const float sscale = p.scale_log2;
+
+    for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
+        const int32_t phys = table[cb / p.block_size];
+        if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+            if (lane == 0) pa::report(p.status, PA_ERR_BOUNDS);
+            continue;
+        }
+        // a chunk never crosses a block: cb and block_size are multiples of 16
+        const int64_t base = (int64_t(phys) * p.block_size + (cb % p.block_size)) * row_elems;
+        const int nvalid = t1 - cb;
+        if (PREFETCH_CHUNKS > 0 && g == 0 && lane == 0) prefetch_chunk(cb + PREFETCH_CHUNKS * wph * CHUNK);
+        // the chunk holding the row this launch wrote: coherent loads through L2
+        const bool coherent = unsigned(new_tok - cb) < unsigned(CHUNK);
+        auto ld = [&](const uint16_t *ptr, bool v) {
+            return !v ? make_uint4(0, 0, 0, 0) : coherent ? __ldcg(reinterpret_cast<const uint4 *>(ptr))
+                                                          : pa::ld_stream16(ptr);
+        };
+        uint4 kr[2][4], vr[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kr[0][j] = ld(kc + base + offk0 + 32 * j, gq < nvalid);
+            kr[1][j] = ld(kc + base + offk1 + 32 * j, 8 + gq < nvalid);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int tok = 2 * tq + (i & 1) + 8 * (i >> 1);
+            const uint16_t *vp = vc + base + tok * row_elems + offv;
+            vr[i][0] = ld(vp, tok < nvalid);
+            vr[i][1] = ld(vp + 64, tok < nvalid);
+        }
+
+        float sc[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+            const uint32_t w[16] = {kr[nb][0].x, kr[nb][0].y, kr[nb][0].z, kr[nb][0].w,
+                                    kr[nb][1].x, kr[nb][1].y, kr[nb][1].z, kr[nb][1].w,
+                                    kr[nb][2].x, kr[nb][2].y, kr[nb][2].z, kr[nb][2].w,
+                                    kr[nb][3].x, kr[nb][3].y, kr[nb][3].z, kr[nb][3].w};
+            sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const uint2 qq = gq < G ? *reinterpret_cast<const uint2 *>(qrow + 32 * (st >> 1) + 4 * (st & 1))
+                                        : make_uint2(0u, 0u);
+                mma_bf16_16816(sc[nb], qq.x, 0u, qq.y, 0u, w[2 * st], w[2 * st + 1]);
+            }
+        }
+
+        float x[4];
+        x[0] = 2 * tq < nvalid ? sc[0][0] * sscale : -INFINITY;
+        x[1] = 2 * tq + 1 < nvalid ? sc[0][1] * sscale : -INFINITY;
+        x[2] = 8 + 2 * tq < nvalid ? sc[1][0] * sscale : -INFINITY;
+        x[3] = 9 + 2 * tq < nvalid ? sc[1][1] * sscale : -INFINITY;
+        float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 1));
+        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 2));
+        // (finite: token 0 of a chunk is always in the split)
+        const bool need = cm > m + FP8_RESCALE_THRESHOLD;
+        if (__any_sync(FULL, need)) {
+            const float m_new = need ? cm : m;
+            const float alpha = pa::sm100::ex2_approx(m - m_new);  // 0 for the first chunk
+            l *= alpha;
+            m = m_new;
+            // the O^T columns of this lane are heads 2tq and 2tq + 1
+            const float a0 = __shfl_sync(FULL, alpha, 8 * tq), a1 = __shfl_sync(FULL, alpha, 8 * tq + 4);
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+                o[mb][0] *= a0;
+                o[mb][1] *= a1;
+                o[mb][2] *= a0;
+                o[mb][3] *= a1;
+            }
+        }
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = pa::sm100::ex2_approx(x[i] - m);
+        float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        ps += __shfl_xor_sync(FULL, ps, 1);
+        ps += __shfl_xor_sync(FULL, ps, 2);
+        l += ps;
+        const uint32_t pb0 = pa::pack_bf16x2(pr[0], pr[1]), pb1 = pa::pack_bf16x2(pr[2], pr[3]);
+        // the words of tokens 2tq (a), 2tq+1 (b), 2tq+8 (c), 2tq+9 (d): word k < 4 holds dims
+        // 8 gq + 2k, 2k+1, word 4 + k dims 64 + 8 gq + 2k, 2k+1
+        const uint32_t wa[8] = {vr[0][0].x, vr[0][0].y, vr[0][0].z, vr[0][0].w, vr[0][1].x, vr[0][1].y, vr[0][1].z, vr[0][1].w};
+        const uint32_t wb[8] = {vr[1][0].x, vr[1][0].y, vr[1][0].z, vr[1][0].w, vr[1][1].x, vr[1][1].y, vr[1][1].z, vr[1][1].w};
+        const uint32_t wc[8] = {vr[2][0].x, vr[2][0].y, vr[2][0].z, vr[2][0].w, vr[2][1].x, vr[2][1].y, vr[2][1].z, vr[2][1].w};
+        const uint32_t wd[8] = {vr[3][0].x, vr[3][0].y, vr[3][0].z, vr[3][0].w, vr[3][1].x, vr[3][1].y, vr[3][1].z, vr[3][1].w};
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+            // dim slot gq: dim 8 gq + mb; slot gq + 8: dim 64 + 8 gq + mb
+            const uint32_t sel = (mb & 1) ? 0x7632u : 0x5410u;
+            const int w0 = mb >> 1, w1 = 4 + (mb >> 1);
+            mma_bf16_16816(o[mb], __byte_perm(wa[w0], wb[w0], sel), __byte_perm(wa[w1], wb[w1], sel),
+                           __byte_perm(wc[w0], wd[w0], sel), __byte_perm(wc[w1], wd[w1], sel), pb0, pb1);
+        }
+    }
+
+    // this CTA's loads are done: the next kernel (the merge) may start launching
+    pa::grid_dependents_launch();
+
+    // every warp's partial through shared memory, over its query staging once
+    // every lane of the warp is done with it; warp g (sub 0) combines the warps
+    // of KV head g
+    __syncwarp();
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int h = 2 * tq + (cc & 1);
+            if (h < G) red_o[warp][h][8 * gq + 64 * (cc >> 1) + mb] = o[mb][cc];
+        }
+    if (tq == 0 && gq < G) {
+        red_ml[warp][gq][0] = m;
+        red_ml[warp][gq][1] = l;
+    }
+    __syncthreads();
+    if (sub != 0 || lane >= 16) return;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float mm = -INFINITY;
+        for (int w = 0; w < wph; ++w) mm = fmaxf(mm, red_ml[g + w * p.kv_heads][h][0]);
+        float ll = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < wph; ++w) {
+            const int ww = g + w * p.kv_heads;
+            const float mw = red_ml[ww][h][0];
+            const float aw = (mw == -INFINITY) ? 0.f : exp2f(mw - mm);
+            ll += red_ml[ww][h][1] * aw;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(red_o[ww][h][8 * c + e], aw, acc[e]);
+        }
+        if (nsplit == 1) {
+            const float inv = p.out_scale / ll;
+            uint4 u;
+            u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + g * G + h) * D + 8 * c) = u;
+        } else {
+            const int64_t row = (int64_t(b) * p.max_splits + s) * p.num_heads + g * G + h;
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + row * D + 8 * c);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (c == 0) p.ws_ml[row] = make_float2(mm, ll);
+        }
+    }
+}
+
 // Merge the split partials of every sequence that has more than one split
 // ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
 // L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.  A thread per
@@ -998,6 +1292,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 // 128-token splits leave many sequences with fewer parts than a cluster has
 // CTAs, were slower in clusters).
 constexpr int CLUSTER_SPLITS = 8;
+// bf16 calls with at least this many query heads per KV head run the MMA kernel
+constexpr int MMA_GROUP_MIN = 4;
 constexpr int CLUSTER_MAX_SPLIT = 1024;
 inline bool use_cluster(bool fp8, int num_seqs, int max_ctx, const Plan &plan)
 {
@@ -1013,6 +1309,12 @@ pa_status launch_split(const DecodeParams &p, bool cluster, cudaStream_t stream)
     if constexpr (FP8) {
         const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
         pa::launch_pdl(decode_fp8_mma_kernel<G>, grid, block, 0, stream, p);
+    } else if constexpr (G >= MMA_GROUP_MIN) {
+        const dim3 grid(unsigned(p.num_seqs), unsigned(p.max_splits > 0 ? p.max_splits : 1));
+        if (p.cos_sin != nullptr)
+            pa::launch_pdl(decode_bf16_mma_kernel<G, true>, grid, block, 0, stream, p);
+        else
+            pa::launch_pdl(decode_bf16_mma_kernel<G, false>, grid, block, 0, stream, p);
     } else if (cluster) {
         const dim3 grid(unsigned(p.num_seqs), unsigned(CLUSTER_SPLITS));
         if (p.cos_sin != nullptr)
@@ -1113,7 +1415,7 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_heads / num_kv_heads;
-    const bool cl = use_cluster(fp8, num_seqs, max_context_len, plan);
+    const bool cl = num_heads / num_kv_heads < MMA_GROUP_MIN && use_cluster(fp8, num_seqs, max_context_len, plan);
     pa_status ls = PA_OK;
     if (fp8) {
         switch (group) {
