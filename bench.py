@@ -60,11 +60,11 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 #   decode: the split kernel (mean of two launches) + the merge kernel of one
 #     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
 #   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
-NCU_TRAFFIC = {"source_sha256": "2a8b07e22aa6c13a00003e900eed219af4f58cbd330d16640f142754af467686",
-               "bytes_per_call": 587_273_984 + 6_572_032 + 10_265_600,
-               "kernel": "decode_split_kernel<2, 0> + decode_merge_kernel"}
-NCU_TRAFFIC_PREFILL = {"source_sha256": "ac044416787c9a2a013e213e087d3a13b8255f708baac09df1bfa71a01fc76cb",
-                       "bytes_per_call": 173_679_360 + 35_962_880, "kernel": "prefill_tc_kernel<0>"}
+NCU_TRAFFIC = {"source_sha256": "7227ddac3b2d2457cd0a3dee9bf68686385ade5de624f9701120dc9fd5397409",
+               "bytes_per_call": 587_302_272 + 6_305_664 + 10_266_624,
+               "kernel": "decode_split_kernel<2, 0, 0> + decode_merge_kernel"}
+NCU_TRAFFIC_PREFILL = {"source_sha256": "7b42f125a443d08fd61d833da8449f862413b698b519fcd78fb46f1e253f66c7",
+                       "bytes_per_call": 166_617_088 + 33_789_184, "kernel": "prefill_tc_kernel<0>"}
 
 
 def _file_sha(path):
@@ -543,6 +543,45 @@ def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6):
     return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512, "kv": "fp8 e4m3, scale 2^-6"}
 
 
+def time_gqa_decode(device, steps, warmup, flush, peak_gbs):
+    """pa_decode_paged on the decode batch's contexts (256 sequences, U[100,
+    1024], block_size 256) with larger query groups: 32 and 64 query heads over
+    8 KV heads (4 and 8 per KV head, the tensor-core decode kernel) beside the
+    16 / 8 of the headline (the CUDA-core kernel).  L2 flushed before each call."""
+    from paged_kv_cache_110_gb300 import binding as pa
+    res = {}
+    ctx = wl.rng(wl.SEED_BASE + 9).integers(100, 1024, size=256, endpoint=True)
+    for hq, hkv in ((16, 8), (32, 8), (64, 8)):
+        b = wl.paged_batch(wl.SEED_BASE + 70, ctx, np.ones_like(ctx), 256, num_heads=hq, num_kv_heads=hkv,
+                           device=device)
+        max_ctx = int(ctx.max())
+        ws = torch.empty(max(pa.pa_decode_workspace_bytes(256, hq, D, max_ctx), 256), dtype=torch.uint8,
+                         device=device)
+        out = torch.empty((256, hq, D), dtype=torch.bfloat16, device=device)
+        bt, cx = torch.as_tensor(b.block_tables, device=device), torch.as_tensor(b.context_lens, device=device)
+
+        def dec():
+            pa.pa_decode_paged(b.tokens.q, b.k_cache, b.v_cache, bt, cx, max_ctx, b.scale, out, ws)
+
+        for _ in range(warmup):
+            dec()
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            dec()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) / 1e3)
+        t = statistics.median(times)
+        gbs = decode_bytes(ctx, 256, num_heads=hq, kv_heads=hkv) / t / 1e9
+        res[f"{hq}q_{hkv}kv"] = {"us": t * 1e6, "gbs": gbs, "frac": gbs / peak_gbs}
+        del b
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_block_size_sweep(device, steps, warmup, flush):
     """Decode (the 256-sequence decode batch) and varlen prefill at block sizes
     16..256: the same contexts and lengths, pools and tables rebuilt per size;
@@ -895,7 +934,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (28 for the headline number)")
     ap.add_argument("--leg", default="all",
-                    choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8",
+                    choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8", "gqa",
                              "block_sizes", "decode_layer"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
     ap.add_argument("--prefill-case", default="all",
@@ -922,6 +961,8 @@ def main():
             res["frac"] = res["gbs"] / peaks["hbm_gbs"]
         elif args.leg == "block_sizes":
             res = time_block_size_sweep(device, max(args.steps, 1), args.warmup, flush)
+        elif args.leg == "gqa":
+            res = time_gqa_decode(device, max(args.steps, 1), args.warmup, flush, peaks["hbm_gbs"])
         elif args.leg == "mixed":
             res = time_mixed(device, max(args.steps, 1), args.warmup, flush)
         elif args.leg == "decode_layer":
@@ -1070,6 +1111,8 @@ def main():
         torch.cuda.empty_cache()
         line["block_sizes"] = time_block_size_sweep(device, 5, 2, flush)
         torch.cuda.empty_cache()
+        line["gqa_decode"] = time_gqa_decode(device, 10, 3, flush, peaks["hbm_gbs"])
+        torch.cuda.empty_cache()
         ld = time_long_decode(device, max(args.steps, 5), 3, flush)
         ld["frac"] = ld["gbs"] / peaks["hbm_gbs"]
         line["long_decode"] = ld
@@ -1090,6 +1133,13 @@ def main():
         import oracle
         oracle.build()
         line["cpu_baseline"] = oracle_sample(host0, meta, target_s=args.cpu_seconds)
+        # the same oracle on one core, a shorter sample
+        all_cores = oracle.num_threads()
+        oracle.set_num_threads(1)
+        one = oracle_sample(host0, meta, target_s=min(5.0, args.cpu_seconds), max_layers=8)
+        oracle.set_num_threads(all_cores)
+        line["cpu_baseline"]["one_core"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                            "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
