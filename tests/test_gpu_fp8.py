@@ -132,6 +132,34 @@ def test_fp8_decode_query_magnitudes(qmul):
     assert_close(out, ref, f"fp8 decode, queries x {qmul}")
 
 
+def test_fp8_decode_bad_block_and_long_context_reported():
+    d = dev()
+    live = np.array([40, 300, 7])
+    batch = wl.paged_batch(wl.SEED_BASE + 87, live, np.ones_like(live), 16, device=d)
+    hist = wl.history_rows(batch.layout, batch.context_lens - batch.query_lens)
+    gk, gv, _, _ = _fp8_pools(batch, 2.0 ** -6, 2.0 ** -6, hist)
+    ws = torch.empty(max(pa().pa_decode_workspace_bytes(3, 16, 128, 300), 256), dtype=torch.uint8, device=d)
+
+    def run(tables, max_ctx):
+        out = torch.full((3, 16, 128), float("nan"), dtype=torch.bfloat16, device=d)
+        st = Status(d)
+        pa().pa_decode_paged_fp8(batch.tokens.q, gk, gv, 2.0 ** -6, 2.0 ** -6, i32(tables, d), i32(live, d), max_ctx,
+                                 batch.scale, out, ws, dev_status=st.t)
+        torch.cuda.synchronize()
+        return out, int(st.t.item())
+
+    out, st = run(batch.block_tables, 300)
+    assert st == 0 and torch.isfinite(out.float()).all()
+    bad = batch.block_tables.copy()
+    bad[1, 3] = -1  # inside sequence 1's live context
+    out_b, st_b = run(bad, 300)
+    assert st_b == pa().PA_ERR_BOUNDS
+    assert torch.equal(out_b[[0, 2]].view(torch.int16), out[[0, 2]].view(torch.int16))  # other rows unchanged
+    out_l, st_l = run(batch.block_tables, 100)  # a context over the stated maximum
+    assert st_l == pa().PA_ERR_BOUNDS
+    assert (out_l[1] == 0).all()
+
+
 def test_fp8_effect_against_the_bf16_oracle():
     # the format's own error: fp8 decode against the bf16 decode of the unquantised data
     batch = wl.decode_batch(device=dev(), num_seqs=64, seed=wl.SEED_BASE + 84)

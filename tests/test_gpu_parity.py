@@ -411,16 +411,19 @@ def test_store_decode_fused_decode_batch_vs_oracle():
     np.testing.assert_array_equal(vg, vb)
 
 
-def test_store_decode_fused_padding_rows_and_bad_block():
+# (16, 8): the CUDA-core decode kernel; (32, 4), (64, 8): the tensor-core one
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4), (64, 8)])
+def test_store_decode_fused_padding_rows_and_bad_block(hq, hkv):
     """Padded sequences (context 0) are neither written nor read; a new-token row whose block id is invalid is
     reported (PA_ERR_BOUNDS) and not written."""
     d = dev()
     ctx = np.array([0, 40, 0, 7])
-    batch = wl.paged_batch(602, ctx, np.minimum(ctx, 1), 16, device=d, table_width=4)
+    batch = wl.paged_batch(602, ctx, np.minimum(ctx, 1), 16, device=d, table_width=4, num_heads=hq,
+                           num_kv_heads=hkv)
     gen = torch.Generator(device="cpu").manual_seed(5)
-    q = torch.randn((4, 16, 128), generator=gen).to(torch.bfloat16).to(d)
-    k_new = torch.randn((4, 8, 128), generator=gen).to(torch.bfloat16).to(d)
-    v_new = torch.randn((4, 8, 128), generator=gen).to(torch.bfloat16).to(d)
+    q = torch.randn((4, hq, 128), generator=gen).to(torch.bfloat16).to(d)
+    k_new = torch.randn((4, hkv, 128), generator=gen).to(torch.bfloat16).to(d)
+    v_new = torch.randn((4, hkv, 128), generator=gen).to(torch.bfloat16).to(d)
     slots = np.array([-1 if c == 0 else batch.layout.slots(b, [c - 1])[0] for b, c in enumerate(ctx)], np.int32)
     kc1, vc1 = batch.k_cache.clone(), batch.v_cache.clone()
     st1 = Status(d)
@@ -442,17 +445,19 @@ def test_store_decode_fused_padding_rows_and_bad_block():
     _store_decode_fused(q, k_new, v_new, kc3, vc3, bad, ctx, batch.scale, st3)
     assert st3.value() == 4
     row3 = slots[3]
-    assert torch.equal(kc3.view(-1, 8, 128)[row3].view(torch.int16),
-                       batch.k_cache.view(-1, 8, 128)[row3].view(torch.int16)), "row with a bad block id was written"
+    assert torch.equal(kc3.view(-1, hkv, 128)[row3].view(torch.int16),
+                       batch.k_cache.view(-1, hkv, 128)[row3].view(torch.int16)), "row with a bad block id was written"
 
 
-def test_decode_padded_rows_and_bounds():
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4), (64, 8)])
+def test_decode_padded_rows_and_bounds(hq, hkv):
     d = dev()
     ctx = np.array([0, 40, 0, 7])
-    batch = wl.paged_batch(601, ctx, np.minimum(ctx, 1), 16, device=d, table_width=4)
+    batch = wl.paged_batch(601, ctx, np.minimum(ctx, 1), 16, device=d, table_width=4, num_heads=hq,
+                           num_kv_heads=hkv)
     kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
     gpu_store(batch, kc, vc)
-    q = torch.randn((4, 16, 128), device=d).to(torch.bfloat16)
+    q = torch.randn((4, hq, 128), device=d).to(torch.bfloat16)
     st = Status(d)
     out = gpu_decode(q, kc, vc, batch.block_tables, ctx, batch.scale, st)
     assert st.value() == 0
