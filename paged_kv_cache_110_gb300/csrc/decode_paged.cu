@@ -1220,9 +1220,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
 // Merge the split partials of every sequence that has more than one split
 // ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
 // L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.  A thread per
-// (head, 8 columns); the statistics and partials of eight splits are loaded
-// together, so that up to eight splits cost one round trip to L2; more are
-// combined eight at a time, the running (M, L, out) rescaled as M grows.
+// (head, 8 columns), 256 threads per CTA and (heads x 16 / 256) CTAs per
+// sequence; the statistics and partials of eight splits are loaded together,
+// so that up to eight splits cost one round trip to L2; more are combined
+// eight at a time, the running (M, L, out) rescaled as M grows.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 {
     pa::grid_dependency_wait();  // the split kernel's partials
@@ -1234,7 +1235,11 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
         return;
     const int nsplit = (ctx + p.split_len - 1) / p.split_len;
     if (nsplit <= 1) return;
-    for (int item = threadIdx.x; item < p.num_heads * (D / 8); item += blockDim.x) {
+    // one (head, 8 columns) item per thread: the grid's y covers the heads
+    // beyond the first 16 (one round trip to L2 whatever the head count)
+    {
+        const int item = int(blockIdx.y * blockDim.x + threadIdx.x);
+        if (item >= p.num_heads * (D / 8)) return;
         const int h = item / (D / 8), c = item % (D / 8);
         const int64_t base = int64_t(b) * p.max_splits * p.num_heads + h;
         constexpr int MS = 8;
@@ -1434,7 +1439,8 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
     }
     if (ls != PA_OK) return ls;
     if (plan.max_splits > 1 && !cl)
-        pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs)), dim3(256), 0, s, p);
+        pa::launch_pdl(decode_merge_kernel, dim3(unsigned(num_seqs), unsigned((num_heads * (D / 8) + 255) / 256)),
+                       dim3(256), 0, s, p);
     return pa::launch_status();
 }
 
