@@ -60,8 +60,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 #   decode: the split kernel (mean of two launches) + the merge kernel of one
 #     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
 #   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
-NCU_TRAFFIC = {"source_sha256": "5b3d10c8d37b5df600b65137730e8e945c44e3d8b3a48e1e2557ff3d4b83910d",
-               "bytes_per_call": 587_287_552 + 6_586_752 + 10_266_752,
+NCU_TRAFFIC = {"source_sha256": "4fd9ad53d69138500e89c931b3ff6b889b8b23695e34c02d42a1e0677164f207",
+               "bytes_per_call": 587_319_168 + 6_407_552 + 10_264_960,
                "kernel": "decode_split_kernel<2, 0, 0> + decode_merge_kernel"}
 NCU_TRAFFIC_PREFILL = {"source_sha256": "7b42f125a443d08fd61d833da8449f862413b698b519fcd78fb46f1e253f66c7",
                        "bytes_per_call": 166_617_088 + 33_789_184, "kernel": "prefill_tc_kernel<0>"}

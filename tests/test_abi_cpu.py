@@ -136,13 +136,13 @@ def test_store_decode_host_checks(lib):
 def test_decode_workspace_follows_the_split_plan(lib):
     """The decode workspace holds fp32 partials [seqs, splits, heads, 128] (256-byte aligned) and a (max, sum)
     pair per (seq, split, head); the keys are split for about 64 CTAs per SM (152 SMs, the GB300 count the
-    library assumes when no GPU is visible) into runs of at least 128 tokens, rounded up to 64; one split needs
-    no workspace."""
+    library assumes when no GPU is visible) into runs of at least 128 tokens (256 from 32 query heads on),
+    rounded up to 64; one split needs no workspace."""
     from paged_kv_cache_110_gb300 import binding as pa
 
     def expect(seqs, heads, ctx, sms=152):
         per_seq = -(-64 * sms // seqs)
-        length = max(-(-(-(-ctx // per_seq)) // 64) * 64, 128)
+        length = max(-(-(-(-ctx // per_seq)) // 64) * 64, 256 if heads >= 32 else 128)
         splits = -(-ctx // length)
         if splits <= 1:
             return 0
@@ -150,11 +150,12 @@ def test_decode_workspace_follows_the_split_plan(lib):
         return -(-n * 512 // 256) * 256 + n * 8
 
     for seqs, heads, ctx in [(256, 16, 1024), (512, 16, 4096), (1, 16, 32768), (64, 16, 100), (1000, 8, 3000),
-                             (3, 32, 129)]:
+                             (3, 32, 129), (256, 64, 1024), (256, 32, 1024), (512, 64, 4096)]:
         assert pa.pa_decode_workspace_bytes(seqs, heads, 128, ctx) == expect(seqs, heads, ctx), (seqs, heads, ctx)
     assert pa.pa_decode_workspace_bytes(256, 16, 128, 1024) == 256 * 8 * 16 * 520   # 8 splits of 128 tokens
     assert pa.pa_decode_workspace_bytes(512, 16, 128, 4096) == 512 * 16 * 16 * 520  # 16 splits of 256 tokens
     assert pa.pa_decode_workspace_bytes(64, 16, 128, 128) == 0                       # one split
+    assert pa.pa_decode_workspace_bytes(256, 64, 128, 1024) == 256 * 4 * 64 * 520   # 4 splits of 256 tokens
 
 
 def test_norm_rope_store_host_checks(lib):
