@@ -1224,9 +1224,13 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
 // ("大模型推理入门与 nano-vLLM 源码详解" §9.5): M = max_s m_s,
 // L = sum_s l_s 2^(m_s - M), out = sum_s o_s 2^(m_s - M) / L.  A thread per
 // (head, 8 columns), 256 threads per CTA and (heads x 16 / 256) CTAs per
-// sequence; the statistics and partials of eight splits are loaded together,
-// so that up to eight splits cost one round trip to L2; more are combined
-// eight at a time, the running (M, L, out) rescaled as M grows.
+// sequence, so the 16 threads of a head are one half-warp.  Per window of 16
+// splits each of them loads one split's (max, sum); M and L are reduced over
+// the half-warp by shuffles, and each split's weight 2^(m_s - M) is handed to
+// the 16 threads by a shuffle as they add that split's 8 columns of o_s.  The
+// statistics and the partials of the window's first eight splits are loaded
+// together (up to eight splits cost one round trip to L2); a later window
+// rescales the running (M, L, out) as M grows.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 {
     pa::grid_dependency_wait();  // the split kernel's partials
@@ -1238,56 +1242,74 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
         return;
     const int nsplit = (ctx + p.split_len - 1) / p.split_len;
     if (nsplit <= 1) return;
-    // one (head, 8 columns) item per thread: the grid's y covers the heads
-    // beyond the first 16 (one round trip to L2 whatever the head count)
-    {
-        const int item = int(blockIdx.y * blockDim.x + threadIdx.x);
-        if (item >= p.num_heads * (D / 8)) return;
-        const int h = item / (D / 8), c = item % (D / 8);
-        const int64_t base = int64_t(b) * p.max_splits * p.num_heads + h;
-        constexpr int MS = 8;
-        float mm = -INFINITY, ll = 0.f;
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int t0 = 0; t0 < nsplit; t0 += MS) {
-            float2 ml[MS];
-            float4 x0[MS], x1[MS];
+    const int item = int(blockIdx.y * blockDim.x + threadIdx.x);
+    // (heads x 16 items: whole half-warps leave here, never part of one)
+    if (item >= p.num_heads * (D / 8)) return;
+    const int h = item / (D / 8), c = item % (D / 8);
+    const int lane = int(threadIdx.x & 31), half0 = lane & 16;
+    const unsigned hmask = 0xffffu << half0;  // this head's half-warp
+    const int64_t base = int64_t(b) * p.max_splits * p.num_heads + h;
+    constexpr int MS = 8;
+    float mm = -INFINITY, ll = 0.f;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int t0 = 0; t0 < nsplit; t0 += 16) {
+        const int nw = min(16, nsplit - t0);
+        const float2 ml = c < nw ? p.ws_ml[base + int64_t(t0 + c) * p.num_heads] : make_float2(-INFINITY, 0.f);
+        float4 x0[MS], x1[MS];
 #pragma unroll
-            for (int u = 0; u < MS; ++u) {
-                if (t0 + u < nsplit) {
-                    const int64_t row = base + int64_t(t0 + u) * p.num_heads;
-                    const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * D + 8 * c);
-                    ml[u] = p.ws_ml[row];
-                    x0[u] = src[0];
-                    x1[u] = src[1];
-                } else {
-                    ml[u] = make_float2(-INFINITY, 0.f);
-                    x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-            float gm = mm;
-#pragma unroll
-            for (int u = 0; u < MS; ++u) gm = fmaxf(gm, ml[u].x);
-            const float a = (mm == -INFINITY) ? 0.f : exp2f(mm - gm);
-            ll *= a;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= a;
-            mm = gm;
-#pragma unroll
-            for (int u = 0; u < MS; ++u) {
-                const float w = (ml[u].x == -INFINITY) ? 0.f : exp2f(ml[u].x - mm);
-                ll += ml[u].y * w;
-                acc[0] += x0[u].x * w; acc[1] += x0[u].y * w; acc[2] += x0[u].z * w; acc[3] += x0[u].w * w;
-                acc[4] += x1[u].x * w; acc[5] += x1[u].y * w; acc[6] += x1[u].z * w; acc[7] += x1[u].w * w;
+        for (int u = 0; u < MS; ++u) {
+            if (u < nw) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(p.ws_o + (base + int64_t(t0 + u) * p.num_heads) * D + 8 * c);
+                x0[u] = src[0];
+                x1[u] = src[1];
+            } else {
+                x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        const float inv = p.out_scale / ll;
-        uint4 u;
-        u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
-        u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + h) * D + 8 * c) = u;
+        float gm = ml.x;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(hmask, gm, o));
+        gm = fmaxf(gm, mm);
+        const float a = (mm == -INFINITY) ? 0.f : exp2f(mm - gm);
+        ll *= a;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= a;
+        mm = gm;
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mm);  // split t0 + c's weight
+        float lw = ml.y * w;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) lw += __shfl_xor_sync(hmask, lw, o);
+        ll += lw;
+        for (int v0 = 0; v0 < nw; v0 += MS) {
+            if (v0 > 0) {  // splits 8 .. 15 of the window
+#pragma unroll
+                for (int u = 0; u < MS; ++u) {
+                    if (v0 + u < nw) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.ws_o + (base + int64_t(t0 + v0 + u) * p.num_heads) * D + 8 * c);
+                        x0[u] = src[0];
+                        x1[u] = src[1];
+                    } else {
+                        x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < MS; ++u) {
+                const float wu = __shfl_sync(hmask, w, half0 | (v0 + u));  // 0 past the window's splits
+                acc[0] += x0[u].x * wu; acc[1] += x0[u].y * wu; acc[2] += x0[u].z * wu; acc[3] += x0[u].w * wu;
+                acc[4] += x1[u].x * wu; acc[5] += x1[u].y * wu; acc[6] += x1[u].z * wu; acc[7] += x1[u].w * wu;
+            }
+        }
     }
+    const float inv = p.out_scale / ll;
+    uint4 u;
+    u.x = pa::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    u.y = pa::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    u.z = pa::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    u.w = pa::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(p.out + (int64_t(b) * p.num_heads + h) * D + 8 * c) = u;
 }
 
 // Long contexts in a large batch: every sequence is split into CLUSTER_SPLITS
