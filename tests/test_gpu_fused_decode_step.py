@@ -105,6 +105,20 @@ def test_fused_step_decode_batch_sampled():
     _check_pool(pools, "fused decode step, decode batch")
 
 
+# Long contexts in a batch large enough for the cluster merge (every sequence
+# split over the eight CTAs of one cluster, merged in distributed shared
+# memory), with the head norm and RoPE fused: sampled sequences against the oracle.
+@pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 256), (8, 8, 64)])
+def test_fused_step_cluster_merge_sampled(hq, hkv, bs):
+    ctx = np.resize(np.array([1, 15, 16, 17, 100, 129, 255, 256, 1000, 2100, 4000, 33]), 96)
+    batch = wl.paged_batch(830 + hq + bs, ctx, np.ones_like(ctx), bs, num_heads=hq, num_kv_heads=hkv, device=dev())
+    seqs = list(range(12)) + [50, 95]
+    out, ref, status, pools, seqs = _run(batch, seqs=seqs, max_positions=4096)
+    assert status == 0
+    assert_close(out[torch.as_tensor(seqs, device=out.device)], ref, f"fused step, cluster merge hq={hq} hkv={hkv}")
+    _check_pool(pools, "fused step, cluster merge")
+
+
 def test_fused_step_rope_only_and_bad_position():
     ctx = np.array([40, 7, 300, 0])
     batch = wl.paged_batch(811, ctx, np.minimum(ctx, 1), 16, device=dev(), table_width=24)
