@@ -629,14 +629,14 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // Decode over E4M3 pools on the warp-level tensor-core MMA (mma.sync
 // m16n8k16: f16 operands, f32 accumulators).
 //
-// Converting every E4M3 code to f32 for CUDA-core FMAs costs more instruction
-// issue than the byte is worth, so fp8 pools would leave HBM idle that way.
-// Here the codes become f16 exactly (every E4M3 value, and that value times
-// 2^-8, is an f16 value): the keys four at a time by a byte permute and a
-// shift (times 2^-8, folded into the score scale and the output scale); the
-// dot products and the P.V sums run as MMAs.
-// The K scale is folded into the score scale and the V scale into the output.  The work split is the bf16 kernel's:
-// CTA = (sequence, split), warp = (KV head, every wph-th 16-token chunk).
+// An fp8 pool halves the bytes but not the work per element, so the decode is
+// bound by instruction issue; converting every code to f32 for CUDA-core FMAs
+// is the costliest way.  Here the codes become f16 exactly (every E4M3 value
+// times 2^-8 is an f16 value), four at a time by a byte permute and a shift,
+// and the dot products and the P.V sums run as MMAs.  The 2^-8 and the K
+// scale are folded into the score scale, the 2^-8 and the V scale into the
+// output scale.  The work split is the bf16 kernel's: CTA = (sequence, split),
+// warp = (KV head, every wph-th 16-token chunk).
 // Lane (gq, tq) = (lane / 4, lane % 4).  Per chunk:
 //   S = Q K^T   A = the group's G query heads (rows 0..G-1 of 16, f16; each
 //               head multiplied by the power of two that puts its largest
@@ -867,13 +867,16 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
                 // two tokens a, b, interleaved (a d0, b d0, a d1, b d1): converted, the
                 // low f16 pair is dim d0's (a, b) and the high pair dim d1's
                 const uint32_t sel = hb ? 0x7362u : 0x5140u;
+                // f0: dim slot gq, tokens 2tq, 2tq+1; f1: slot gq + 8; f2, f3: the same
+                // for tokens 2tq+8, 2tq+9
                 uint32_t f0[2], f1[2], f2[2], f3[2];
-                e4m3x4_to_f16x2x2(__byte_perm(va[i], vb[i], sel), f0[0], f0[1]);          // dim slot gq, tokens 2tq, 2tq+1
-                e4m3x4_to_f16x2x2(__byte_perm(va[i + 2], vb[i + 2], sel), f1[0], f1[1]);  // slot gq + 8
-                e4m3x4_to_f16x2x2(__byte_perm(vcw[i], vd[i], sel), f2[0], f2[1]);         // slot gq, tokens 2tq+8, 2tq+9
+                e4m3x4_to_f16x2x2(__byte_perm(va[i], vb[i], sel), f0[0], f0[1]);
+                e4m3x4_to_f16x2x2(__byte_perm(va[i + 2], vb[i + 2], sel), f1[0], f1[1]);
+                e4m3x4_to_f16x2x2(__byte_perm(vcw[i], vd[i], sel), f2[0], f2[1]);
                 e4m3x4_to_f16x2x2(__byte_perm(vcw[i + 2], vd[i + 2], sel), f3[0], f3[1]);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) mma_16816(o[4 * i + 2 * hb + jj], f0[jj], f1[jj], f2[jj], f3[jj], pb0, pb1);
+                for (int jj = 0; jj < 2; ++jj)
+                    mma_16816(o[4 * i + 2 * hb + jj], f0[jj], f1[jj], f2[jj], f3[jj], pb0, pb1);
             }
         }
     }
@@ -1155,10 +1158,15 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
         const uint32_t pb0 = pa::pack_bf16x2(pr[0], pr[1]), pb1 = pa::pack_bf16x2(pr[2], pr[3]);
         // the words of tokens 2tq (a), 2tq+1 (b), 2tq+8 (c), 2tq+9 (d): word k < 4 holds dims
         // 8 gq + 2k, 2k+1, word 4 + k dims 64 + 8 gq + 2k, 2k+1
-        const uint32_t wa[8] = {vr[0][0].x, vr[0][0].y, vr[0][0].z, vr[0][0].w, vr[0][1].x, vr[0][1].y, vr[0][1].z, vr[0][1].w};
-        const uint32_t wb[8] = {vr[1][0].x, vr[1][0].y, vr[1][0].z, vr[1][0].w, vr[1][1].x, vr[1][1].y, vr[1][1].z, vr[1][1].w};
-        const uint32_t wc[8] = {vr[2][0].x, vr[2][0].y, vr[2][0].z, vr[2][0].w, vr[2][1].x, vr[2][1].y, vr[2][1].z, vr[2][1].w};
-        const uint32_t wd[8] = {vr[3][0].x, vr[3][0].y, vr[3][0].z, vr[3][0].w, vr[3][1].x, vr[3][1].y, vr[3][1].z, vr[3][1].w};
+        auto words = [&](int t, uint32_t (&w8)[8]) {
+            w8[0] = vr[t][0].x; w8[1] = vr[t][0].y; w8[2] = vr[t][0].z; w8[3] = vr[t][0].w;
+            w8[4] = vr[t][1].x; w8[5] = vr[t][1].y; w8[6] = vr[t][1].z; w8[7] = vr[t][1].w;
+        };
+        uint32_t wa[8], wb[8], wc[8], wd[8];
+        words(0, wa);
+        words(1, wb);
+        words(2, wc);
+        words(3, wd);
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
             // dim slot gq: dim 8 gq + mb; slot gq + 8: dim 64 + 8 gq + mb
