@@ -273,7 +273,10 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
  * max_context_len <= 8192 and at least four cluster CTAs per SM), inside one
  * thread-block cluster per sequence (eight equal splits, merged in
  * distributed shared memory), which leaves the workspace untouched.  Either
- * way the caller passes a workspace of the size below.
+ * way the caller passes a workspace of the size below.  Arithmetic: scores,
+ * softmax statistics and the weighted sums in fp32; with 4 or 8 query heads
+ * per KV head the dot products and P.V run on tensor cores (bf16 operands,
+ * fp32 accumulation, P rounded to bf16), otherwise on CUDA cores in fp32.
  *
  *   q             [num_seqs, num_heads, head_dim] bf16, seq stride
  *                 q_stride_seq elements.
@@ -381,7 +384,11 @@ pa_status pa_store_kvcache_fp8(const void *k, int64_t k_stride_tok, const void *
  * pa_decode_paged_fp8: pa_decode_paged over fp8 pools written by
  * pa_store_kvcache_fp8, with K_j = E4M3 value * k_scale and V_j = E4M3 value *
  * v_scale.  Same arguments, workspace (pa_decode_workspace_bytes) and errors
- * as pa_decode_paged; half the bytes per context token.
+ * as pa_decode_paged; half the bytes per context token.  The codes are
+ * converted to f16 exactly and multiplied on tensor cores with fp32
+ * accumulation: q enters as an f16 value (each head scaled by a power of two,
+ * undone on the score, so any normal bf16 query is exact), P is rounded to
+ * f16 for P.V.
  */
 pa_status pa_decode_paged_fp8(const void *q, int64_t q_stride_seq, const void *k_cache, const void *v_cache,
                               float k_scale, float v_scale, int64_t num_blocks, int block_size,
