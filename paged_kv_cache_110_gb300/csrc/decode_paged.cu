@@ -236,6 +236,35 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
+// Before a decode CTA waits on the previous kernel: bring the first chunk
+// (16 rows of every KV head) of each of its warp groups into L2, so that the
+// first loads after the wait find them there.  The context length and the
+// block id read here may still be written by the previous kernel (the kernel
+// reads both again after the wait); validated, they serve only as the address
+// of an L2 prefetch, which changes no result.  cluster_parts > 0: the
+// sequence is cut into that many equal parts, else into the call's splits.
+__device__ __forceinline__ void prefetch_first_chunks(const DecodeParams &p, int elem_bytes, int cluster_parts)
+{
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) != 0 || warp % p.kv_heads != 0) return;
+    const int b = blockIdx.x, s = blockIdx.y;
+    const int ctx = p.context_lens[b];
+    if (ctx <= 0 || ctx > p.max_ctx || int64_t(ctx) > int64_t(p.max_blocks) * p.block_size) return;
+    const int split_len = cluster_parts > 0
+                              ? ((ctx + cluster_parts - 1) / cluster_parts + CHUNK - 1) / CHUNK * CHUNK
+                              : p.split_len;
+    const int t0 = s * split_len, t1 = min(ctx, t0 + split_len);
+    const int cf = t0 + (warp / p.kv_heads) * CHUNK;
+    if (cf >= t1) return;
+    const int32_t pf = p.block_table[int64_t(b) * p.max_blocks + cf / p.block_size];
+    if (pf < 0 || int64_t(pf) >= p.num_blocks) return;
+    const int64_t row_bytes = int64_t(p.kv_heads) * D * elem_bytes;
+    const int64_t off = (int64_t(pf) * p.block_size + cf % p.block_size) * row_bytes;
+    const uint32_t bytes = uint32_t(min(CHUNK, t1 - cf) * row_bytes);  // (a multiple of 128)
+    pa::sm100::prefetch_l2_bulk(static_cast<const char *>(p.k_cache) + off, bytes);
+    pa::sm100::prefetch_l2_bulk(static_cast<const char *>(p.v_cache) + off, bytes);
+}
+
 template <int G, bool ROPE, bool CLUSTER>
 __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodeParams p)
 {
@@ -245,6 +274,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
     const int b = blockIdx.x, s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, c = lane & 15;
+    if constexpr (!CLUSTER) prefetch_first_chunks(p, int(sizeof(typename KV::Elem)), 0);
     // launched programmatically: everything below may depend on the previous
     // kernel (the KV write of this step's token)
     pa::grid_dependency_wait();
@@ -314,20 +344,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
         }
     }
 
-    if (g == 0 && lane == 0) {
-        // bring this warp group's first chunk (all KV heads, one contiguous run) into L2
-        const int cf = t0 + sub * CHUNK;
-        if (cf < t1) {
-            const int32_t pf = table[cf / p.block_size];
-            if (pf >= 0 && int64_t(pf) < p.num_blocks) {
-                const int64_t r = (int64_t(pf) * p.block_size + cf % p.block_size) * row_elems;
-                const uint32_t bytes = uint32_t(min(CHUNK, t1 - cf) * row_elems * sizeof(typename KV::Elem));
-                const uint32_t b16 = (bytes + 15u) & ~15u;
-                pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.k_cache) + r, b16);
-                pa::sm100::prefetch_l2_bulk(static_cast<const typename KV::Elem *>(p.v_cache) + r, b16);
-            }
-        }
-    }
+    // (a cluster's CTAs prefetch after the wait: measured 0.4% faster on long contexts)
+    if constexpr (CLUSTER) prefetch_first_chunks(p, int(sizeof(typename KV::Elem)), int(gridDim.y));
     float qf[G][8];
     {
         uint4 qr[G];
@@ -968,6 +986,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
     const int half = lane >> 4, c = lane & 15;
+    prefetch_first_chunks(p, 2, 0);
     // launched programmatically: everything below may depend on the previous
     // kernel (the KV write of this step's token)
     pa::grid_dependency_wait();
@@ -1035,7 +1054,6 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
         pa::sm100::prefetch_l2_bulk(kc + r, b16);
         pa::sm100::prefetch_l2_bulk(vc + r, b16);
     };
-    if (g == 0 && lane == 0) prefetch_chunk(t0 + sub * CHUNK);
 
     // the group's query heads, this warp's slice of the merge buffer as staging
     __shared__ __align__(16) float red_o[NW][G][D];
