@@ -679,18 +679,43 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // the prescale gives); P (below 2^8) is rounded to f16 (relative 2^-11) for
 // the P.V MMA.
 
-// The four E4M3 codes of w as two f16 pairs (codes 0, 1 and codes 2, 3), each
-// value times 2^-8, exactly: with the sign bits taken out, a byte permute puts
-// each code's seven low bits in the low byte of a 16-bit lane and its sign as
-// bit 0 of the lane's high byte; a shift left by 7 then moves eeee mmm to where
-// an f16 keeps the low four exponent bits and the top three mantissa bits
-// (the f16 exponent bias, 15, exceeds E4M3's, 7, by 8: the 2^-8; E4M3
-// subnormals land on f16 subnormals) and the sign to bit 15.
+// Two E4M3 codes as an f16 pair, each value times 2^-8, exactly.  One byte
+// permute takes the two codes (bytes `sel` picks from a and b) into the low
+// bytes of the two 16-bit lanes and fills each lane's high byte with copies of
+// that code's sign bit (the permute's sign-replicate selectors, bit 3 of a
+// selector nibble); a shift left by 7 then puts eeee mmm where an f16 keeps
+// the low four exponent bits and the top three mantissa bits, and one copy of
+// the sign at bit 15.  The mask clears what else the shift moved in: the code's
+// own sign at bit 14 (the top exponent bit, which stays 0) and the low lane's
+// other sign copies at the high lane's bits 0-6.  The f16 exponent bias, 15,
+// exceeds E4M3's, 7, by 8: the 2^-8; E4M3 subnormals land on f16 subnormals.
+// sel: 0x9180 for bytes 0, 1 of a; 0xB3A2 for bytes 2, 3 of a; 0xC480 + 0x1111 i
+// for byte i of a and byte i of b.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "n"(SEL));
+    return (r << 7) & 0xbf80bf80u;
+}
+
+// Byte k of a and byte k of b as an f16 pair, for k = 2hb and 2hb + 1.
+__device__ __forceinline__ void e4m3_byte_pairs(uint32_t a, uint32_t b, int hb, uint32_t (&f)[2])
+{
+    if (hb == 0) {
+        f[0] = e4m3x2_to_f16x2<0xC480u>(a, b);
+        f[1] = e4m3x2_to_f16x2<0xD591u>(a, b);
+    } else {
+        f[0] = e4m3x2_to_f16x2<0xE6A2u>(a, b);
+        f[1] = e4m3x2_to_f16x2<0xF7B3u>(a, b);
+    }
+}
+
+// The four E4M3 codes of w as two f16 pairs (codes 0, 1 and codes 2, 3).
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    const uint32_t mag = w & 0x7f7f7f7fu, sgn = (w >> 7) & 0x01010101u;
-    lo = __byte_perm(mag, sgn, 0x5140u) << 7;
-    hi = __byte_perm(mag, sgn, 0x7362u) << 7;
+    lo = e4m3x2_to_f16x2<0x9180u>(w, 0u);
+    hi = e4m3x2_to_f16x2<0xB3A2u>(w, 0u);
 }
 
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
@@ -881,17 +906,14 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
         for (int i = 0; i < 2; ++i) {
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                // bytes 2hb, 2hb+1 of word i (dims 4i + 2hb + {0,1} of the lane's 16) of
-                // two tokens a, b, interleaved (a d0, b d0, a d1, b d1): converted, the
-                // low f16 pair is dim d0's (a, b) and the high pair dim d1's
-                const uint32_t sel = hb ? 0x7362u : 0x5140u;
-                // f0: dim slot gq, tokens 2tq, 2tq+1; f1: slot gq + 8; f2, f3: the same
-                // for tokens 2tq+8, 2tq+9
+                // [jj]: byte 2hb + jj of word i (dim 4i + 2hb + jj of the lane's 16) of
+                // two tokens as an f16 pair; f0: dim slot gq, tokens 2tq, 2tq+1; f1:
+                // slot gq + 8; f2, f3: the same for tokens 2tq+8, 2tq+9
                 uint32_t f0[2], f1[2], f2[2], f3[2];
-                e4m3x4_to_f16x2x2(__byte_perm(va[i], vb[i], sel), f0[0], f0[1]);
-                e4m3x4_to_f16x2x2(__byte_perm(va[i + 2], vb[i + 2], sel), f1[0], f1[1]);
-                e4m3x4_to_f16x2x2(__byte_perm(vcw[i], vd[i], sel), f2[0], f2[1]);
-                e4m3x4_to_f16x2x2(__byte_perm(vcw[i + 2], vd[i + 2], sel), f3[0], f3[1]);
+                e4m3_byte_pairs(va[i], vb[i], hb, f0);
+                e4m3_byte_pairs(va[i + 2], vb[i + 2], hb, f1);
+                e4m3_byte_pairs(vcw[i], vd[i], hb, f2);
+                e4m3_byte_pairs(vcw[i + 2], vd[i + 2], hb, f3);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj)
                     mma_16816(o[4 * i + 2 * hb + jj], f0[jj], f1[jj], f2[jj], f3[jj], pb0, pb1);
