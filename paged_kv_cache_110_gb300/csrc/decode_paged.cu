@@ -733,6 +733,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The transpose of an 8 x 8 matrix of 16-bit values held as the warp holds an
+// MMA fragment (lane 4r + c: row r, columns 2c, 2c + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 constexpr float FP8_RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 template <int G>
@@ -815,6 +824,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
             qa[st][1] = f16x2_of(x[4 * st + 2] * up, x[4 * st + 3] * up);
         }
     }
+    // the score scales of this lane's S^T columns, heads 2tq and 2tq + 1
+    const float ss0 = __shfl_sync(FULL, sscale, 8 * tq), ss1 = __shfl_sync(FULL, sscale, 8 * tq + 4);
 
     // this lane's byte offsets within a chunk's first row of head g: its two
     // 16-byte pieces of a key row lie 64 bytes apart and the four lanes of a
@@ -825,7 +836,9 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
     float o[8][4];  // O^T: block mb holds dims 16 gq + mb (o[mb][0..1]) and 16 gq + 8 + mb (o[mb][2..3])
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
-    float m = -INFINITY, l = 0.f;  // head gq
+    // heads 2tq, 2tq + 1: running max (the same in the 8 lanes of a tq) and this
+    // lane's share of the sum (its tokens), added up over the 8 lanes at the end
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
     for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
         const int32_t phys = table[cb / p.block_size];
@@ -853,37 +866,45 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
             vr[i] = tok < nvalid ? pa::ld_stream16(vc + base + tok * row_elems + offv) : make_uint4(0, 0, 0, 0);
         }
 
-        float sc[2][4];
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-            const uint32_t w[8] = {kr[nb][0].x, kr[nb][0].y, kr[nb][0].z, kr[nb][0].w,
-                                   kr[nb][1].x, kr[nb][1].y, kr[nb][1].z, kr[nb][1].w};
-            sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+        // S^T = K Q^T: one MMA per 16-dim step covers the chunk's 16 tokens
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint32_t w0[8] = {kr[0][0].x, kr[0][0].y, kr[0][0].z, kr[0][0].w,
+                                    kr[0][1].x, kr[0][1].y, kr[0][1].z, kr[0][1].w};
+            const uint32_t w1[8] = {kr[1][0].x, kr[1][0].y, kr[1][0].z, kr[1][0].w,
+                                    kr[1][1].x, kr[1][1].y, kr[1][1].z, kr[1][1].w};
 #pragma unroll
             for (int st = 0; st < 8; ++st) {
-                uint32_t b0, b1;
-                e4m3x4_to_f16x2x2(w[st], b0, b1);
-                mma_16816(sc[nb], qa[st][0], 0u, qa[st][1], 0u, b0, b1);
+                uint32_t a0, a1, a2, a3;  // tokens gq (a0, a2) and gq + 8 (a1, a3)
+                e4m3x4_to_f16x2x2(w0[st], a0, a2);
+                e4m3x4_to_f16x2x2(w1[st], a1, a3);
+                mma_16816(sc, a0, a1, a2, a3, qa[st][0], qa[st][1]);
             }
         }
 
+        // sc: tokens gq (0, 1) and gq + 8 (2, 3), heads 2tq (0, 2) and 2tq + 1 (1, 3)
         float x[4];
-        x[0] = 2 * tq < nvalid ? sc[0][0] * sscale : -INFINITY;
-        x[1] = 2 * tq + 1 < nvalid ? sc[0][1] * sscale : -INFINITY;
-        x[2] = 8 + 2 * tq < nvalid ? sc[1][0] * sscale : -INFINITY;
-        x[3] = 9 + 2 * tq < nvalid ? sc[1][1] * sscale : -INFINITY;
-        float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 1));
-        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 2));
-        // (finite: token 0 of a chunk is always in the split)
-        const bool need = cm > m + FP8_RESCALE_THRESHOLD;
-        if (__any_sync(FULL, need)) {
-            const float m_new = need ? cm : m;
-            const float alpha = pa::sm100::ex2_approx(m - m_new);  // 0 for the first chunk
-            l *= alpha;
-            m = m_new;
-            // the O^T columns of this lane are heads 2tq and 2tq + 1
-            const float a0 = __shfl_sync(FULL, alpha, 8 * tq), a1 = __shfl_sync(FULL, alpha, 8 * tq + 4);
+        x[0] = gq < nvalid ? sc[0] * ss0 : -INFINITY;
+        x[1] = gq < nvalid ? sc[1] * ss1 : -INFINITY;
+        x[2] = gq + 8 < nvalid ? sc[2] * ss0 : -INFINITY;
+        x[3] = gq + 8 < nvalid ? sc[3] * ss1 : -INFINITY;
+        float cm0 = fmaxf(x[0], x[2]), cm1 = fmaxf(x[1], x[3]);
+        if (__any_sync(FULL, cm0 > m0 + FP8_RESCALE_THRESHOLD || cm1 > m1 + FP8_RESCALE_THRESHOLD)) {
+            // the chunk's max of each head over its 8 lanes (finite: token 0 of a
+            // chunk is always in the split)
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                cm0 = fmaxf(cm0, __shfl_xor_sync(FULL, cm0, off));
+                cm1 = fmaxf(cm1, __shfl_xor_sync(FULL, cm1, off));
+            }
+            const float n0 = cm0 > m0 + FP8_RESCALE_THRESHOLD ? cm0 : m0;
+            const float n1 = cm1 > m1 + FP8_RESCALE_THRESHOLD ? cm1 : m1;
+            const float a0 = pa::sm100::ex2_approx(m0 - n0), a1 = pa::sm100::ex2_approx(m1 - n1);  // 0 at first
+            l0 *= a0;
+            l1 *= a1;
+            m0 = n0;
+            m1 = n1;
+            // the O^T columns of this lane are the same heads
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
                 o[mb][0] *= a0;
@@ -893,13 +914,16 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
             }
         }
         float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = pa::sm100::ex2_approx(x[i] - m);
-        float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-        ps += __shfl_xor_sync(FULL, ps, 1);
-        ps += __shfl_xor_sync(FULL, ps, 2);
-        l += ps;
-        const uint32_t pb0 = f16x2_of(pr[0], pr[1]), pb1 = f16x2_of(pr[2], pr[3]);
+        pr[0] = pa::sm100::ex2_approx(x[0] - m0);
+        pr[1] = pa::sm100::ex2_approx(x[1] - m1);
+        pr[2] = pa::sm100::ex2_approx(x[2] - m0);
+        pr[3] = pa::sm100::ex2_approx(x[3] - m1);
+        l0 += pr[0] + pr[2];
+        l1 += pr[1] + pr[3];
+        // P^T as the B operand of the P.V MMA wants tokens 2tq, 2tq + 1 of head gq
+        // in a lane: the transpose of each 8 x 8 tile of P as the lanes hold it
+        const uint32_t pb0 = movmatrix_trans(f16x2_of(pr[0], pr[1]));
+        const uint32_t pb1 = movmatrix_trans(f16x2_of(pr[2], pr[3]));
         const uint32_t va[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w}, vb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
         const uint32_t vcw[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, vd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
 #pragma unroll
@@ -935,9 +959,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
             const int h = 2 * tq + (cc & 1);
             if (h < G) red_o[warp][h][16 * gq + 8 * (cc >> 1) + mb] = o[mb][cc];
         }
-    if (tq == 0 && gq < G) {
-        red_ml[warp][gq][0] = m;
-        red_ml[warp][gq][1] = l;
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        l0 += __shfl_xor_sync(FULL, l0, off);
+        l1 += __shfl_xor_sync(FULL, l1, off);
+    }
+    if (gq == 0 && 2 * tq < G) {
+        red_ml[warp][2 * tq][0] = m0;
+        red_ml[warp][2 * tq][1] = l0;
+    }
+    if (gq == 0 && 2 * tq + 1 < G) {
+        red_ml[warp][2 * tq + 1][0] = m1;
+        red_ml[warp][2 * tq + 1][1] = l1;
     }
     __syncthreads();
     if (sub != 0 || lane >= 16) return;
