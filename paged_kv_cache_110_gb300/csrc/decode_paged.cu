@@ -1147,7 +1147,9 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
     float o[8][4];  // O^T: block mb holds dims 8 gq + mb (o[mb][0..1]) and 64 + 8 gq + mb (o[mb][2..3])
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
-    float m = -INFINITY, l = 0.f;  // head gq
+    // heads 2tq, 2tq + 1: running max (the same in the 8 lanes of a tq) and this
+    // lane's share of the sum (its tokens), added up over the 8 lanes at the end
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const float sscale = p.scale_log2;
 
     for (int cb = t0 + sub * CHUNK; cb < t1; cb += wph * CHUNK) {
@@ -1180,39 +1182,49 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
             vr[i][1] = ld(vp + 64, tok < nvalid);
         }
 
-        float sc[2][4];
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-            const uint32_t w[16] = {kr[nb][0].x, kr[nb][0].y, kr[nb][0].z, kr[nb][0].w,
-                                    kr[nb][1].x, kr[nb][1].y, kr[nb][1].z, kr[nb][1].w,
-                                    kr[nb][2].x, kr[nb][2].y, kr[nb][2].z, kr[nb][2].w,
-                                    kr[nb][3].x, kr[nb][3].y, kr[nb][3].z, kr[nb][3].w};
-            sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+        // S^T = K Q^T: one MMA per 16-dim step covers the chunk's 16 tokens
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint32_t w0[16] = {kr[0][0].x, kr[0][0].y, kr[0][0].z, kr[0][0].w,
+                                     kr[0][1].x, kr[0][1].y, kr[0][1].z, kr[0][1].w,
+                                     kr[0][2].x, kr[0][2].y, kr[0][2].z, kr[0][2].w,
+                                     kr[0][3].x, kr[0][3].y, kr[0][3].z, kr[0][3].w};
+            const uint32_t w1[16] = {kr[1][0].x, kr[1][0].y, kr[1][0].z, kr[1][0].w,
+                                     kr[1][1].x, kr[1][1].y, kr[1][1].z, kr[1][1].w,
+                                     kr[1][2].x, kr[1][2].y, kr[1][2].z, kr[1][2].w,
+                                     kr[1][3].x, kr[1][3].y, kr[1][3].z, kr[1][3].w};
 #pragma unroll
             for (int st = 0; st < 8; ++st) {
                 const uint2 qq = gq < G ? *reinterpret_cast<const uint2 *>(qrow + 32 * (st >> 1) + 4 * (st & 1))
                                         : make_uint2(0u, 0u);
-                mma_bf16_16816(sc[nb], qq.x, 0u, qq.y, 0u, w[2 * st], w[2 * st + 1]);
+                // A: tokens gq (words 2st, 2st + 1) and gq + 8; B: head gq's query
+                mma_bf16_16816(sc, w0[2 * st], w1[2 * st], w0[2 * st + 1], w1[2 * st + 1], qq.x, qq.y);
             }
         }
 
+        // sc: tokens gq (0, 1) and gq + 8 (2, 3), heads 2tq (0, 2) and 2tq + 1 (1, 3)
         float x[4];
-        x[0] = 2 * tq < nvalid ? sc[0][0] * sscale : -INFINITY;
-        x[1] = 2 * tq + 1 < nvalid ? sc[0][1] * sscale : -INFINITY;
-        x[2] = 8 + 2 * tq < nvalid ? sc[1][0] * sscale : -INFINITY;
-        x[3] = 9 + 2 * tq < nvalid ? sc[1][1] * sscale : -INFINITY;
-        float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 1));
-        cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, 2));
-        // (finite: token 0 of a chunk is always in the split)
-        const bool need = cm > m + FP8_RESCALE_THRESHOLD;
-        if (__any_sync(FULL, need)) {
-            const float m_new = need ? cm : m;
-            const float alpha = pa::sm100::ex2_approx(m - m_new);  // 0 for the first chunk
-            l *= alpha;
-            m = m_new;
-            // the O^T columns of this lane are heads 2tq and 2tq + 1
-            const float a0 = __shfl_sync(FULL, alpha, 8 * tq), a1 = __shfl_sync(FULL, alpha, 8 * tq + 4);
+        x[0] = gq < nvalid ? sc[0] * sscale : -INFINITY;
+        x[1] = gq < nvalid ? sc[1] * sscale : -INFINITY;
+        x[2] = gq + 8 < nvalid ? sc[2] * sscale : -INFINITY;
+        x[3] = gq + 8 < nvalid ? sc[3] * sscale : -INFINITY;
+        float cm0 = fmaxf(x[0], x[2]), cm1 = fmaxf(x[1], x[3]);
+        if (__any_sync(FULL, cm0 > m0 + FP8_RESCALE_THRESHOLD || cm1 > m1 + FP8_RESCALE_THRESHOLD)) {
+            // the chunk's max of each head over its 8 lanes (finite: token 0 of a
+            // chunk is always in the split)
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                cm0 = fmaxf(cm0, __shfl_xor_sync(FULL, cm0, off));
+                cm1 = fmaxf(cm1, __shfl_xor_sync(FULL, cm1, off));
+            }
+            const float n0 = cm0 > m0 + FP8_RESCALE_THRESHOLD ? cm0 : m0;
+            const float n1 = cm1 > m1 + FP8_RESCALE_THRESHOLD ? cm1 : m1;
+            const float a0 = pa::sm100::ex2_approx(m0 - n0), a1 = pa::sm100::ex2_approx(m1 - n1);  // 0 at first
+            l0 *= a0;
+            l1 *= a1;
+            m0 = n0;
+            m1 = n1;
+            // the O^T columns of this lane are the same heads
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
                 o[mb][0] *= a0;
@@ -1222,13 +1234,15 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
             }
         }
         float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = pa::sm100::ex2_approx(x[i] - m);
-        float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-        ps += __shfl_xor_sync(FULL, ps, 1);
-        ps += __shfl_xor_sync(FULL, ps, 2);
-        l += ps;
-        const uint32_t pb0 = pa::pack_bf16x2(pr[0], pr[1]), pb1 = pa::pack_bf16x2(pr[2], pr[3]);
+        pr[0] = pa::sm100::ex2_approx(x[0] - m0);
+        pr[1] = pa::sm100::ex2_approx(x[1] - m1);
+        pr[2] = pa::sm100::ex2_approx(x[2] - m0);
+        pr[3] = pa::sm100::ex2_approx(x[3] - m1);
+        l0 += pr[0] + pr[2];
+        l1 += pr[1] + pr[3];
+        // P^T as the B operand of the P.V MMA: the transpose of each 8 x 8 tile
+        const uint32_t pb0 = movmatrix_trans(pa::pack_bf16x2(pr[0], pr[1]));
+        const uint32_t pb1 = movmatrix_trans(pa::pack_bf16x2(pr[2], pr[3]));
         // the words of tokens 2tq (a), 2tq+1 (b), 2tq+8 (c), 2tq+9 (d): word k < 4 holds dims
         // 8 gq + 2k, 2k+1, word 4 + k dims 64 + 8 gq + 2k, 2k+1
         auto words = [&](int t, uint32_t (&w8)[8]) {
@@ -1264,9 +1278,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_bf16_mma_kernel(const Decod
             const int h = 2 * tq + (cc & 1);
             if (h < G) red_o[warp][h][8 * gq + 64 * (cc >> 1) + mb] = o[mb][cc];
         }
-    if (tq == 0 && gq < G) {
-        red_ml[warp][gq][0] = m;
-        red_ml[warp][gq][1] = l;
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        l0 += __shfl_xor_sync(FULL, l0, off);
+        l1 += __shfl_xor_sync(FULL, l1, off);
+    }
+    if (gq == 0 && 2 * tq < G) {
+        red_ml[warp][2 * tq][0] = m0;
+        red_ml[warp][2 * tq][1] = l0;
+    }
+    if (gq == 0 && 2 * tq + 1 < G) {
+        red_ml[warp][2 * tq + 1][0] = m1;
+        red_ml[warp][2 * tq + 1][1] = l1;
     }
     __syncthreads();
     if (sub != 0 || lane >= 16) return;
