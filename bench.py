@@ -470,12 +470,12 @@ def time_prefill(device, steps, warmup, flush, only="all"):
     return res
 
 
-def time_long_decode(device, steps, warmup, flush):
+def time_long_decode(device, steps, warmup, flush, seqs=512):
     from paged_kv_cache_110_gb300 import binding as pa
-    batch = wl.long_decode(device=device)
+    batch = wl.long_decode(device=device, num_seqs=seqs)
     max_ctx = int(batch.context_lens.max())
-    ws = torch.empty(max(pa.pa_decode_workspace_bytes(512, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
-    out = torch.empty((512, HQ, D), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(seqs, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
+    out = torch.empty((seqs, HQ, D), dtype=torch.bfloat16, device=device)
     bt = torch.as_tensor(batch.block_tables, device=device)
     ctx = torch.as_tensor(batch.context_lens, device=device)
     sl = torch.as_tensor(batch.slot_mapping, device=device)
@@ -494,15 +494,15 @@ def time_long_decode(device, steps, warmup, flush):
     t = statistics.median(times)
     nbytes = decode_bytes(batch.context_lens, 256)
     del batch
-    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512}
+    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": seqs}
 
 
-def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6):
+def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6, seqs=512):
     """The long-decode workload over fp8 (E4M3) pools: the bf16 pool's history
     and the new tokens quantised by pa_store_kvcache_fp8, then
     pa_decode_paged_fp8 timed with L2 flushed before each call."""
     from paged_kv_cache_110_gb300 import binding as pa
-    batch = wl.long_decode(device=device)
+    batch = wl.long_decode(device=device, num_seqs=seqs)
     shape = batch.k_cache.shape
     k8 = torch.empty(shape, dtype=torch.uint8, device=device)
     v8 = torch.empty(shape, dtype=torch.uint8, device=device)
@@ -516,8 +516,8 @@ def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6):
                             torch.as_tensor(batch.slot_mapping, device=device))
     max_ctx = int(batch.context_lens.max())
     ctx_np = batch.context_lens
-    ws = torch.empty(max(pa.pa_decode_workspace_bytes(512, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
-    out = torch.empty((512, HQ, D), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(seqs, HQ, D, max_ctx), 256), dtype=torch.uint8, device=device)
+    out = torch.empty((seqs, HQ, D), dtype=torch.bfloat16, device=device)
     bt = torch.as_tensor(batch.block_tables, device=device)
     ctx = torch.as_tensor(ctx_np, device=device)
     q = batch.tokens.q
@@ -540,7 +540,7 @@ def time_long_decode_fp8(device, steps, warmup, flush, scale=2.0 ** -6):
         times.append(s.elapsed_time(e) / 1e3)
     t = statistics.median(times)
     nbytes = decode_bytes(ctx_np, 256, kv_elem_bytes=1)
-    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": 512, "kv": "fp8 e4m3, scale 2^-6"}
+    return {"gbs": nbytes / t / 1e9, "ms": t * 1e3, "bytes": nbytes, "seqs": seqs, "kv": "fp8 e4m3, scale 2^-6"}
 
 
 def time_gqa_decode(device, steps, warmup, flush, peak_gbs):
@@ -937,6 +937,9 @@ def main():
                     choices=["all", "prefill", "long_decode", "rope_store", "metadata", "mixed", "fp8", "gqa",
                              "block_sizes", "decode_layer"],
                     help="run one secondary leg alone (profiling); prints that leg's results only")
+    ap.add_argument("--long-seqs", type=int, default=512,
+                    help="sequences of the long-decode legs run alone (--leg long_decode / fp8); fewer give the "
+                         "small case of the same shape for a profiler capture")
     ap.add_argument("--prefill-case", default="all",
                     choices=["all", "varlen_16k", "prefix_2048_chunked", "chunk_512_over_8k"])
     args = ap.parse_args()
@@ -957,7 +960,7 @@ def main():
         if args.leg == "prefill":
             res = time_prefill(device, max(args.steps, 1), args.warmup, flush, args.prefill_case)
         elif args.leg == "fp8":
-            res = time_long_decode_fp8(device, max(args.steps, 1), args.warmup, flush)
+            res = time_long_decode_fp8(device, max(args.steps, 1), args.warmup, flush, seqs=args.long_seqs)
             res["frac"] = res["gbs"] / peaks["hbm_gbs"]
         elif args.leg == "block_sizes":
             res = time_block_size_sweep(device, max(args.steps, 1), args.warmup, flush)
@@ -974,7 +977,7 @@ def main():
             for v in res.values():
                 v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         else:
-            res = time_long_decode(device, max(args.steps, 1), args.warmup, flush)
+            res = time_long_decode(device, max(args.steps, 1), args.warmup, flush, seqs=args.long_seqs)
         if rank == 0:
             print(json.dumps({"leg": args.leg, "results": res}), flush=True)
         return 0

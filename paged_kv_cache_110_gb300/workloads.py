@@ -305,10 +305,12 @@ def prefix_chunk(device="cpu"):
 
 def long_decode(device="cpu", num_seqs=512, seed=SEED_BASE + 5) -> PagedBatch:
     """Long-context max-batch decode: 512 sequences, context_lens U[1024,
-    4096], block_size 256, fully fragmented tables over an 8192-block pool
-    (about 8.6 GB of K+V per layer)."""
+    4096], block_size 256, fully fragmented tables over a pool of 16 blocks per
+    sequence (8192 blocks, about 8.6 GB of K+V per layer, for 512; fewer
+    sequences give the small case of the same shape that a profiler capture
+    needs)."""
     ctx = rng(seed + 7).integers(1024, 4096, size=num_seqs, endpoint=True)
-    return paged_batch(seed, ctx, np.ones_like(ctx), 256, num_blocks=8192, device=device)
+    return paged_batch(seed, ctx, np.ones_like(ctx), 256, num_blocks=16 * num_seqs, device=device)
 
 
 # ----------------------------------------------------------------- head norm and RoPE inputs
