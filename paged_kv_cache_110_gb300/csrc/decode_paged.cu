@@ -75,6 +75,10 @@ struct DecodeParams {
     int split_len;
     int max_splits;
     int32_t *status;
+    // 128, the factor that moves a permuted E4M3 code into f16 position (a
+    // multiply read from the parameters issues on the FMA pipe; a shift by a
+    // constant would load the ALU pipe, the busiest of the fp8 decode)
+    uint32_t code_mul;
 };
 
 struct Plan {
@@ -691,31 +695,32 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // exceeds E4M3's, 7, by 8: the 2^-8; E4M3 subnormals land on f16 subnormals.
 // sel: 0x9180 for bytes 0, 1 of a; 0xB3A2 for bytes 2, 3 of a; 0xC480 + 0x1111 i
 // for byte i of a and byte i of b.
+// mul: 128 (the shift by 7), passed in so that it stays a multiply.
 template <uint32_t SEL>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t a, uint32_t b)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t a, uint32_t b, uint32_t mul)
 {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "n"(SEL));
-    return (r << 7) & 0xbf80bf80u;
+    return (r * mul) & 0xbf80bf80u;
 }
 
 // Byte k of a and byte k of b as an f16 pair, for k = 2hb and 2hb + 1.
-__device__ __forceinline__ void e4m3_byte_pairs(uint32_t a, uint32_t b, int hb, uint32_t (&f)[2])
+__device__ __forceinline__ void e4m3_byte_pairs(uint32_t a, uint32_t b, int hb, uint32_t (&f)[2], uint32_t mul)
 {
     if (hb == 0) {
-        f[0] = e4m3x2_to_f16x2<0xC480u>(a, b);
-        f[1] = e4m3x2_to_f16x2<0xD591u>(a, b);
+        f[0] = e4m3x2_to_f16x2<0xC480u>(a, b, mul);
+        f[1] = e4m3x2_to_f16x2<0xD591u>(a, b, mul);
     } else {
-        f[0] = e4m3x2_to_f16x2<0xE6A2u>(a, b);
-        f[1] = e4m3x2_to_f16x2<0xF7B3u>(a, b);
+        f[0] = e4m3x2_to_f16x2<0xE6A2u>(a, b, mul);
+        f[1] = e4m3x2_to_f16x2<0xF7B3u>(a, b, mul);
     }
 }
 
 // The four E4M3 codes of w as two f16 pairs (codes 0, 1 and codes 2, 3).
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi, uint32_t mul)
 {
-    lo = e4m3x2_to_f16x2<0x9180u>(w, 0u);
-    hi = e4m3x2_to_f16x2<0xB3A2u>(w, 0u);
+    lo = e4m3x2_to_f16x2<0x9180u>(w, 0u, mul);
+    hi = e4m3x2_to_f16x2<0xB3A2u>(w, 0u, mul);
 }
 
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi)
@@ -876,8 +881,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
 #pragma unroll
             for (int st = 0; st < 8; ++st) {
                 uint32_t a0, a1, a2, a3;  // tokens gq (a0, a2) and gq + 8 (a1, a3)
-                e4m3x4_to_f16x2x2(w0[st], a0, a2);
-                e4m3x4_to_f16x2x2(w1[st], a1, a3);
+                e4m3x4_to_f16x2x2(w0[st], a0, a2, p.code_mul);
+                e4m3x4_to_f16x2x2(w1[st], a1, a3, p.code_mul);
                 mma_16816(sc, a0, a1, a2, a3, qa[st][0], qa[st][1]);
             }
         }
@@ -934,10 +939,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
                 // two tokens as an f16 pair; f0: dim slot gq, tokens 2tq, 2tq+1; f1:
                 // slot gq + 8; f2, f3: the same for tokens 2tq+8, 2tq+9
                 uint32_t f0[2], f1[2], f2[2], f3[2];
-                e4m3_byte_pairs(va[i], vb[i], hb, f0);
-                e4m3_byte_pairs(va[i + 2], vb[i + 2], hb, f1);
-                e4m3_byte_pairs(vcw[i], vd[i], hb, f2);
-                e4m3_byte_pairs(vcw[i + 2], vd[i + 2], hb, f3);
+                e4m3_byte_pairs(va[i], vb[i], hb, f0, p.code_mul);
+                e4m3_byte_pairs(va[i + 2], vb[i + 2], hb, f1, p.code_mul);
+                e4m3_byte_pairs(vcw[i], vd[i], hb, f2, p.code_mul);
+                e4m3_byte_pairs(vcw[i + 2], vd[i + 2], hb, f3, p.code_mul);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj)
                     mma_16816(o[4 * i + 2 * hb + jj], f0[jj], f1[jj], f2[jj], f3[jj], pb0, pb1);
@@ -1546,6 +1551,7 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
     p.split_len = plan.split_len;
     p.max_splits = plan.max_splits;
     p.status = dev_status;
+    p.code_mul = 128u;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_heads / num_kv_heads;
