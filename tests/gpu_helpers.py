@@ -120,3 +120,24 @@ def compact_pool(tables, ctx, seqs, kc, vc, block_size):
     ids = torch.as_tensor(np.concatenate(rows).astype(np.int64), device=kc.device)
     return (wl.bf16_bits(kc.index_select(0, ids)).copy(), wl.bf16_bits(vc.index_select(0, ids)).copy(),
             np.array(new_tables))
+
+
+def grow_keys(batch, growth):
+    """Scores that grow along the key positions: every query made |q| and every
+    key (the history rows in the pool and the new tokens) set to growth times
+    its position, in every head, so that each later chunk of keys scores higher
+    than the ones before and the online softmax keeps moving its maximum."""
+    lay = batch.layout
+    rows, pos = [], []
+    for b, (c, n) in enumerate(zip(batch.context_lens, batch.query_lens)):
+        h = int(c) - int(n)
+        rows.append(lay.slots(b, np.arange(h)))
+        pos.append(np.arange(h))
+    rows, pos = np.concatenate(rows), np.concatenate(pos)
+    d = batch.k_cache.device
+    kv = batch.k_cache.view(-1, batch.k_cache.shape[2], batch.k_cache.shape[3])
+    val = (growth * torch.as_tensor(pos, dtype=torch.float32, device=d))[:, None, None]
+    kv[torch.as_tensor(rows, device=d)] = val.expand(-1, kv.shape[1], kv.shape[2]).to(torch.bfloat16)
+    new_pos = torch.as_tensor(batch.positions, dtype=torch.float32, device=d)
+    batch.tokens.k.copy_((growth * new_pos)[:, None, None].expand_as(batch.tokens.k).to(torch.bfloat16))
+    batch.tokens.q.copy_(batch.tokens.q.abs())

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import MAX_ABS, MEAN_ABS, Status, assert_close, dev, i32, pa
+from gpu_helpers import MAX_ABS, MEAN_ABS, Status, assert_close, dev, grow_keys, i32, pa
 from paged_kv_cache_110_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -119,6 +119,21 @@ def test_fp8_decode_head_layouts(hq, hkv, bs):
                            num_kv_heads=hkv, device=dev())
     out, ref, _ = _decode_case(batch, 2.0 ** -6, 2.0 ** -5)
     assert_close(out, ref, f"fp8 decode hq={hq} hkv={hkv} bs={bs}")
+
+
+# scores that grow along the keys (every key = growth * position, q >= 0; K
+# scale 2^-3 keeps the largest key, 42, inside E4M3's range): the running
+# maximum of each head moves every few chunks (0.02) or rarely (0.002), in
+# every lane, for group sizes 2, 8 and 8 with a single KV head
+@pytest.mark.parametrize("growth", [0.02, 0.002], ids=["fast_growth", "slow_growth"])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 4), (8, 1)])
+def test_fp8_decode_growing_scores_rescale(growth, hq, hkv):
+    live = np.array([700, 1024, 129, 300, 1600, 17, 2100, 40])
+    batch = wl.paged_batch(wl.SEED_BASE + 88 + hq, live, np.ones_like(live), 64, num_heads=hq, num_kv_heads=hkv,
+                           device=dev())
+    grow_keys(batch, growth)
+    out, ref, _ = _decode_case(batch, 2.0 ** -3, 2.0 ** -5)
+    assert_close(out, ref, f"fp8 decode, growing scores x {growth}, hq={hq} hkv={hkv}")
 
 
 # queries far from unit size: a bf16 query of any normal magnitude enters the

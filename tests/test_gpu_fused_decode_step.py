@@ -85,7 +85,8 @@ def _check_pool(pools, what):
     _rows_close(rows_g[live], rows_b[live], what)
 
 
-@pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 16), (16, 8, 256), (8, 1, 64), (32, 4, 128), (4, 2, 48)])
+@pytest.mark.parametrize("hq,hkv,bs", [(16, 8, 16), (16, 8, 256), (8, 1, 64), (32, 4, 128), (4, 2, 48),
+                                       (16, 4, 32)])
 def test_fused_step_matches_oracle(hq, hkv, bs):
     ctx = np.array([1, 15, 16, 17, 255, 256, 257, 1000, 33])
     batch = wl.paged_batch(800 + hq + bs, ctx, np.ones_like(ctx), bs, num_heads=hq, num_kv_heads=hkv, device=dev())

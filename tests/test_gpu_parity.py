@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (MAX_ABS, MEAN_ABS, Status, assert_close, compact_pool, dev, gpu_decode, gpu_prefill, gpu_store, i32,
-                         oracle_prefill, oracle_store, pa, prefill_workspace)
+from gpu_helpers import (MAX_ABS, MEAN_ABS, Status, assert_close, compact_pool, dev, gpu_decode, gpu_prefill, gpu_store,
+                         grow_keys, i32, oracle_prefill, oracle_store, pa, prefill_workspace)
 from oracle_cases import bits
 from paged_kv_cache_110_gb300 import workloads as wl
 
@@ -342,6 +342,23 @@ def test_decode_cluster_merge(hq, hkv, bs):
     assert st.value() == 0
     assert torch.equal(fused.view(torch.int16), out.view(torch.int16))
     assert torch.equal(kf.view(torch.int16), kc.view(torch.int16)) and torch.equal(vf.view(torch.int16), vc.view(torch.int16))
+
+
+# Scores that grow along the keys (every key = growth * position, q >= 0):
+# with growth 0.02 a 16-token chunk scores about 4 higher (log2 units) than
+# the one before, so every decode kernel moves its running maximum (and
+# rescales O) every few chunks, in every lane; with 0.002 it runs on a stale
+# maximum for many chunks.  The CUDA-core kernel (16 q heads), the tensor-core
+# kernel (32 and 64 q heads over 8) and the cluster merge (96 long sequences).
+@pytest.mark.parametrize("growth", [0.02, 0.002], ids=["fast_growth", "slow_growth"])
+@pytest.mark.parametrize("hq,hkv,nseq", [(16, 8, 8), (32, 8, 8), (64, 8, 8), (16, 8, 96)],
+                         ids=["cuda_core", "mma_g4", "mma_g8", "cluster"])
+def test_decode_growing_scores_rescale(growth, hq, hkv, nseq):
+    ctx = np.resize(np.array([700, 1024, 129, 300, 1600, 17, 2100, 40]), nseq)
+    batch = wl.paged_batch(wl.SEED_BASE + 47 + hq + nseq, ctx, np.ones_like(ctx), 64, num_heads=hq,
+                           num_kv_heads=hkv, device=dev())
+    grow_keys(batch, growth)
+    _decode_vs_oracle(batch)
 
 
 def _store_decode_fused(q, k_new, v_new, kc, vc, tables, ctx, scale, status, max_ctx=None):
