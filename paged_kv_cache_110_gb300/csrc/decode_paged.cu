@@ -86,18 +86,28 @@ struct Plan {
     int max_splits;
 };
 
-Plan make_plan(int num_seqs, int max_ctx, int num_heads)
+// CTAs per SM the split plan aims at: bf16 pools, and fp8 pools, whose tokens
+// carry half the bytes, so that a split's fixed work (its query, its partial
+// and its share of the merge) weighs twice as much (measured on 512 x U[1k,
+// 4k] contexts: 470 us per fp8 call at 16, 473 at 32, 487 at 64).  Fewer CTAs
+// per SM never give more splits, so the workspace size pa_decode_workspace_bytes
+// returns (the bf16 plan) covers the fp8 plan too.
+constexpr int PLAN_CTAS_PER_SM = 64;
+constexpr int PLAN_CTAS_PER_SM_FP8 = 16;
+
+Plan make_plan(int num_seqs, int max_ctx, int num_heads, int ctas_per_sm = PLAN_CTAS_PER_SM)
 {
     Plan p{CHUNK, 0};
     if (num_seqs <= 0 || max_ctx <= 0) return p;
     // Many CTAs keep enough loads in flight (about 64 per SM measured best for
-    // long contexts), but a split shorter than 128 tokens costs more in
-    // fixed work and partials than it gains (measured on 1k contexts), and
-    // shorter than 256 from 32 query heads on, whose partials and merge grow
-    // with the head count (measured: 64 q heads over 8 KV heads 5% faster).
-    // The plan depends only on the call's arguments and the device's SM count.
+    // long contexts over bf16 pools), but a split shorter than 128 tokens costs
+    // more in fixed work and partials than it gains (measured on 1k contexts),
+    // and shorter than 256 from 32 query heads on, whose partials and merge
+    // grow with the head count (measured: 64 q heads over 8 KV heads 5%
+    // faster).  The plan depends only on the call's arguments and the device's
+    // SM count.
     const int sms = pa::num_sms() > 0 ? pa::num_sms() : 152;
-    const long long target_ctas = 64LL * sms;
+    const long long target_ctas = (long long)ctas_per_sm * sms;
     long long per_seq = (target_ctas + num_seqs - 1) / num_seqs;
     if (per_seq < 1) per_seq = 1;
     long long len = (max_ctx + per_seq - 1) / per_seq;
@@ -1512,7 +1522,7 @@ pa_status decode_impl(const void *q, int64_t q_stride_seq, const void *k_cache, 
                               max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_heads,
                               num_kv_heads, head_dim, out);
     if (st != PA_OK || num_seqs == 0) return st;
-    const Plan plan = make_plan(num_seqs, max_context_len, num_heads);
+    const Plan plan = make_plan(num_seqs, max_context_len, num_heads, fp8 ? PLAN_CTAS_PER_SM_FP8 : PLAN_CTAS_PER_SM);
     if (plan.max_splits > 65535) return PA_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes(num_seqs, num_heads, plan);
     if (need > 0 && (workspace == nullptr || workspace_bytes_given < need || !pa::aligned(workspace, 256)))
