@@ -60,8 +60,8 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 #   decode: the split kernel (mean of two launches) + the merge kernel of one
 #     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
 #   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
-NCU_TRAFFIC = {"source_sha256": "ead6381f40af73a2fec235711ded9b917a44f8f2f4425a43d29afd7ed84fc309",
-               "bytes_per_call": 587_355_008 + 6_149_504 + 10_268_928,
+NCU_TRAFFIC = {"source_sha256": "7637c97dcdb80289b1e4d024207b306460d9c553b880178c79e2a945def9d1a1",
+               "bytes_per_call": 587_439_488 + 6_371_968 + 10_270_208,
                "kernel": "decode_split_kernel<2, 0, 0> + decode_merge_kernel"}
 NCU_TRAFFIC_PREFILL = {"source_sha256": "7b42f125a443d08fd61d833da8449f862413b698b519fcd78fb46f1e253f66c7",
                        "bytes_per_call": 166_617_088 + 33_789_184, "kernel": "prefill_tc_kernel<0>"}
