@@ -56,20 +56,45 @@ ROW_BYTES = HKV * D * 2  # one token's K (or V) row of one layer
 
 # DRAM traffic per call from ncu captures (dram__bytes_read.sum +
 # dram__bytes_write.sum; one-pass metrics, clock control off), valid only
-# while the kernel's source file is unchanged:
+# while the code of the kernel's source file is unchanged (the key hashes the
+# file with its comments and whitespace taken out, so that a comment edit
+# keeps the capture and any code edit drops it):
 #   decode: the split kernel (mean of two launches) + the merge kernel of one
 #     pa_store_decode_paged call, decode-batch workload (2 layers, eager pass);
 #   prefill: one prefill_tc_kernel launch of the varlen-prefill workload.
-NCU_TRAFFIC = {"source_sha256": "7637c97dcdb80289b1e4d024207b306460d9c553b880178c79e2a945def9d1a1",
+NCU_TRAFFIC = {"code_sha256": "b527dbc7cb18d8b9cd31c12ccf83ae5106d8c6842ddc2b4636f2328a155b8b60",
                "bytes_per_call": 587_439_488 + 6_371_968 + 10_270_208,
                "kernel": "decode_split_kernel<2, 0, 0> + decode_merge_kernel"}
-NCU_TRAFFIC_PREFILL = {"source_sha256": "7b42f125a443d08fd61d833da8449f862413b698b519fcd78fb46f1e253f66c7",
+NCU_TRAFFIC_PREFILL = {"code_sha256": "5783926236cbd97f4ba27b9a10d83c8eb239572fc08ae3829f819de54f61be4e",
                        "bytes_per_call": 166_617_088 + 33_789_184, "kernel": "prefill_tc_kernel<0>"}
 
 
-def _file_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def _code_sha(path):
+    """sha256 of a C / CUDA source's code: comments removed (string and
+    character literals kept whole), then every run of whitespace made one
+    space."""
+    with open(path, encoding="utf-8") as f:
+        src = f.read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return hashlib.sha256(" ".join("".join(out).split()).encode()).hexdigest()
 
 
 # ----------------------------------------------------------------- distributed
@@ -1054,7 +1079,7 @@ def main():
     del e2e_graph
 
     src = os.path.join(ROOT, "paged_kv_cache_110_gb300", "csrc", "decode_paged.cu")
-    traffic = NCU_TRAFFIC["bytes_per_call"] if NCU_TRAFFIC["source_sha256"] == _file_sha(src) else None
+    traffic = NCU_TRAFFIC["bytes_per_call"] if NCU_TRAFFIC["code_sha256"] == _code_sha(src) else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
@@ -1108,7 +1133,7 @@ def main():
             "frac": vp["tflops"] / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 dense (burst)",
             "algorithmic_flops_per_call": vp["gflop"] * 1e9, "us_per_call": vp["ms"] * 1e3,
             "counted": "4 * 128 * 16 FLOP per visible (query, key) pair; masked pairs and padding not counted",
-            "traffic": NCU_TRAFFIC_PREFILL["bytes_per_call"] if NCU_TRAFFIC_PREFILL["source_sha256"] == _file_sha(
+            "traffic": NCU_TRAFFIC_PREFILL["bytes_per_call"] if NCU_TRAFFIC_PREFILL["code_sha256"] == _code_sha(
                 os.path.join(ROOT, "paged_kv_cache_110_gb300", "csrc", "prefill_paged.cu")) else None,
             "traffic_unit": "bytes per call (DRAM read + write, ncu)"}
         torch.cuda.empty_cache()

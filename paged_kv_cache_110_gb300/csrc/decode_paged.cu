@@ -661,33 +661,37 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_split_kernel(const DecodePa
 // Decode over E4M3 pools on the warp-level tensor-core MMA (mma.sync
 // m16n8k16: f16 operands, f32 accumulators).
 //
-// An fp8 pool halves the bytes but not the work per element, so the decode is
-// bound by instruction issue; converting every code to f32 for CUDA-core FMAs
+// An fp8 pool halves the bytes but not the work per element: every code must
+// become an MMA operand, and converting every code to f32 for CUDA-core FMAs
 // is the costliest way.  Here the codes become f16 exactly (every E4M3 value
-// times 2^-8 is an f16 value), four at a time by a byte permute and a shift,
-// and the dot products and the P.V sums run as MMAs.  The 2^-8 and the K
-// scale are folded into the score scale, the 2^-8 and the V scale into the
+// times 2^-8 is an f16 value), two at a time by a byte permute, a shift and a
+// mask, and the dot products and the P.V sums run as MMAs.  The 2^-8 and the
+// K scale are folded into the score scale, the 2^-8 and the V scale into the
 // output scale.  The work split is the bf16 kernel's: CTA = (sequence, split),
 // warp = (KV head, every wph-th 16-token chunk).
 // Lane (gq, tq) = (lane / 4, lane % 4).  Per chunk:
-//   S = Q K^T   A = the group's G query heads (rows 0..G-1 of 16, f16; each
-//               head multiplied by the power of two that puts its largest
-//               magnitude in [2^13, 2^14), undone on the fp32 score), B = the
-//               keys of an 8-token block; two blocks x 8 steps of 16 dims.
-//               Lane (gq, tq) supplies token gq of a block, dims 16 tq .. + 15
-//               and 64 + 16 tq .. + 15: each step takes four of them (one
-//               word), the query the same, and the four lanes of a token read
-//               adjacent 16-byte pieces.
-//   softmax     the accumulator holds head gq's scores of tokens 2tq, 2tq+1
-//               and 8+2tq, 9+2tq: max and sum over the 4 lanes of head gq.
-//               The running max moves only when a score passes it by more than
-//               2^8 (log2 units), so O is rarely rescaled; O / l uses the same
-//               max, so the result does not depend on when it moved.
+//   S^T = K Q^T   A = the keys of the chunk's 16 tokens (f16), 8 steps of 16
+//               dims: lane (gq, tq) supplies tokens gq and gq + 8, dims
+//               16 tq .. + 15 and 64 + 16 tq .. + 15 (each step takes four of
+//               them, one word per token), and the four lanes of a token read
+//               adjacent 16-byte pieces; B = the group's G query heads as
+//               columns 0..G-1 of 8 (f16, the same dims; each head multiplied
+//               by the power of two that puts its largest magnitude in
+//               [2^13, 2^14), undone on the fp32 score).  One MMA per step.
+//   softmax     the accumulator holds the scores of tokens gq and gq + 8 for
+//               heads 2tq and 2tq + 1 (columns past G are zero and unused).
+//               The running max of a head, the same in its 8 lanes, moves only
+//               when a score passes it by more than 2^8 (log2 units): only
+//               then are the 8 lanes' maxima reduced by shuffles and O
+//               rescaled; each lane keeps its share of the sum, added up over
+//               the 8 lanes at the end.  O / l uses the same max, so the result
+//               does not depend on when it moved.
 //   O^T += V^T P^T   A = V^T (16 dims x the 16 tokens): lane gq supplies dims
 //               16 gq .. 16 gq + 15 of tokens 2tq, 2tq+1, 2tq+8, 2tq+9, two
-//               tokens' codes interleaved by a byte permute before the
-//               conversion; B = P^T (f16), which is the S accumulator's layout
-//               as it stands; C = O^T, 8 blocks of 16 dims x 8 head columns.
+//               tokens' codes paired by the conversion's byte permute; B = P^T
+//               (f16): each 8 x 8 tile of P as the S^T accumulator holds it,
+//               transposed by movmatrix; C = O^T, 8 blocks of 16 dims x 8 head
+//               columns, heads 2tq and 2tq + 1 in lane (gq, tq) as in S^T.
 // Rounding: the products of f16 operands are exact in the f32 accumulators
 // (q is a bf16 value times a power of two, exactly an f16 value in the range
 // the prescale gives); P (below 2^8) is rounded to f16 (relative 2^-11) for
@@ -1027,16 +1031,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_fp8_mma_kernel(const Decode
 //
 // The CUDA-core kernel keeps G x 8 partial dot products, G x 8 query values
 // and G x 8 outputs per lane; from G = 4 on they no longer fit its register
-// budget and spill.  Here S = Q K^T and O^T += V^T P^T run as MMAs laid out
-// as the fp8 kernel's (see there): lane (gq, tq) = (lane / 4, lane % 4)
-// supplies token gq of each 8-token block of a 16-token chunk, dims 32 j + 8 tq
-// .. + 7 for j < 4 (the pool's bf16 words are the B registers as they are, the
-// query taken in the same dim order; the four lanes of a token read adjacent
-// 16-byte pieces), and dims 8 gq .. + 7 and 64 + 8 gq .. + 7 of tokens 2tq,
-// 2tq+1, 2tq+8, 2tq+9 for P.V (two tokens' values of one dim paired by a byte
-// permute).  The query (with the head norm and RoPE when fused) is
-// formed in the half-warp layout of the CUDA-core kernel and staged through
-// shared memory into the A fragments.  P is rounded to bf16 for the P.V MMA.
+// budget and spill.  Here S^T = K Q^T and O^T += V^T P^T run as MMAs laid
+// out as the fp8 kernel's (see there): lane (gq, tq) = (lane / 4, lane % 4)
+// supplies tokens gq and gq + 8 of a 16-token chunk, dims 32 j + 8 tq .. + 7
+// for j < 4 (the pool's bf16 words are the A registers as they are, the query,
+// the B operand, taken in the same dim order; the four lanes of a token read
+// adjacent 16-byte pieces), and dims 8 gq .. + 7 and 64 + 8 gq .. + 7 of
+// tokens 2tq, 2tq+1, 2tq+8, 2tq+9 for P.V (two tokens' values of one dim
+// paired by a byte permute).  The softmax is the fp8 kernel's (heads 2tq and
+// 2tq + 1 per lane, P^T by movmatrix).  The query (with the head norm and RoPE
+// when fused) is formed in the half-warp layout of the CUDA-core kernel and
+// staged through shared memory, from which the B fragments are read at every
+// chunk.  P is rounded to bf16 for the P.V MMA.
 // The fused KV write, the split partials and the output are the CUDA-core
 // kernel's.
 

@@ -65,3 +65,19 @@ def test_reference_arm_under_torchrun_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_key_ignores_comments_not_code(tmp_path):
+    """The ncu traffic figures are keyed to a hash of the kernel source's code:
+    comment and whitespace edits keep the key, a code edit (even inside a
+    string literal that holds comment markers) changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text('int x = 1; // one\n/* block */ asm("mov.u32 %0, 1; // in a string" : "=r"(x));\nchar c = \'\\\'\';\n')
+    b = tmp_path / "b.cu"
+    b.write_text('int x = 1;\n\n   asm("mov.u32 %0, 1; // in a string" : "=r"(x)); // another\nchar c = \'\\\'\';')
+    c = tmp_path / "c.cu"
+    c.write_text('int x = 1; // one\n/* block */ asm("mov.u32 %0, 2; // in a string" : "=r"(x));\nchar c = \'\\\'\';\n')
+    assert bench._code_sha(str(a)) == bench._code_sha(str(b))
+    assert bench._code_sha(str(a)) != bench._code_sha(str(c))
