@@ -256,8 +256,10 @@ void pa_test_stall_pipelines(long long cycles);
 
 /*
  * Bytes of scratch pa_decode_paged needs for these host-side sizes on the
- * current device (it depends on the device's SM count).  Returns 0 when the
- * arguments are invalid.
+ * current device (it depends on the device's SM count).  pa_decode_paged_fp8
+ * cuts contexts into no more splits than pa_decode_paged (its splits are
+ * longer: its tokens carry half the bytes), so the same size serves it.
+ * Returns 0 when the arguments are invalid.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
 
